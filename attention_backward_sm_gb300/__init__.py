@@ -1,0 +1,159 @@
+"""Python binding of libfabwd.so: single-pass flash-attention backward on GB300.
+
+The functions keep the C names of ``include/fabwd.h`` and only marshal
+arguments (data pointers, sizes, the current CUDA stream).  Every step of
+the computation runs in the library's CUDA kernels; PyTorch provides device
+memory and streams.  ``backward`` chains the three backward calls and
+allocates their outputs with torch.
+
+Tensors: q, o, do, dq are [total_q, H, d] bf16; k, v, dk, dv are
+[total_kv, H, d] bf16; m, l, D are [total_q, H] float32; cu_q / cu_kv are
+cumulative int32 offsets (B+1 entries) given both as a CUDA tensor and as a
+host sequence.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_DQ_ATOMIC = 0
+FA_DQ_DETERMINISTIC = 1
+
+
+class FabwdError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"fabwd error {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    return _lib.load()
+
+
+def fa_last_error() -> str:
+    return (lib().fa_last_error() or b"").decode()
+
+
+def _check(rc: int):
+    if rc != FA_OK:
+        raise FabwdError(rc, fa_last_error())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _host_offsets(cu) -> np.ndarray:
+    if isinstance(cu, torch.Tensor):
+        cu = cu.detach().cpu().numpy()
+    a = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
+    return a
+
+
+def _hp(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _shape(q):
+    total, heads, dim = q.shape
+    return int(total), int(heads), int(dim)
+
+
+def fa_fwd_stats(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
+                 stream=None):
+    """Fills o (bf16), m and l (fp32) in place."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv = int(k.shape[0])
+    _check(lib().fa_fwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(m), _ptr(l), _ptr(cu_q_dev),
+                              _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1, total_q, total_kv, heads, dim,
+                              int(bool(causal)), float(scale), _stream(stream)))
+
+
+def fa_bwd_preprocess(o, do, D, dq_acc, stream=None):
+    total_q, heads, dim = _shape(o)
+    _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(D), _ptr(dq_acc), total_q, heads, dim,
+                                   _stream(stream)))
+
+
+def fa_bwd_workspace_size(cu_q_host, cu_kv_host, heads: int, head_dim: int, causal: bool, dq_mode: int) -> int:
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    n = lib().fa_bwd_workspace_size(_hp(cq), _hp(ck), len(cq) - 1, heads, head_dim, int(bool(causal)), dq_mode)
+    err = fa_last_error()
+    if err:
+        raise FabwdError(FA_ERR_INVALID_ARG, err)
+    return int(n)
+
+
+def fa_bwd(q, k, v, do, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool,
+           scale: float, dq_mode: int = FA_DQ_ATOMIC, workspace=None, stream=None):
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv = int(k.shape[0])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(m), _ptr(l), _ptr(D), _ptr(dq_acc), _ptr(dk),
+                        _ptr(dv), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1, total_q, total_kv,
+                        heads, dim, int(bool(causal)), float(scale), int(dq_mode), _ptr(workspace), ws_bytes,
+                        _stream(stream)))
+
+
+def fa_bwd_dq_finalize(dq_acc, dq, scale: float, stream=None):
+    total_q, heads, dim = _shape(dq)
+    _check(lib().fa_bwd_dq_finalize(_ptr(dq_acc), _ptr(dq), total_q, heads, dim, float(scale), _stream(stream)))
+
+
+def fa_check_device_status(stream=None):
+    _check(lib().fa_check_device_status(_stream(stream)))
+
+
+def forward_stats(q, k, v, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float, stream=None):
+    """Allocates and returns (o, m, l) from fa_fwd_stats."""
+    total_q, heads, dim = _shape(q)
+    o = torch.zeros_like(q)
+    m = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
+    l = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
+    fa_fwd_stats(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal, scale, stream)
+    return o, m, l
+
+
+class Workspace:
+    """Device buffers one backward needs besides its inputs and outputs."""
+
+    def __init__(self, q, cu_q_host, cu_kv_host, causal, dq_mode):
+        total_q, heads, dim = _shape(q)
+        self.D = torch.empty((total_q, heads), dtype=torch.float32, device=q.device)
+        self.dq_acc = torch.empty((total_q, heads, dim), dtype=torch.float32, device=q.device)
+        n = fa_bwd_workspace_size(cu_q_host, cu_kv_host, heads, dim, causal, dq_mode)
+        self.ws = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device) if n > 0 else None
+
+
+def backward(q, k, v, o, do, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
+             dq_mode: int = FA_DQ_ATOMIC, out=None, work: Workspace | None = None, stream=None):
+    """preprocess -> fa_bwd -> finalize on one stream; returns (dq, dk, dv)."""
+    if work is None:
+        work = Workspace(q, cu_q_host, cu_kv_host, causal, dq_mode)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    fa_bwd_preprocess(o, do, work.D, work.dq_acc, stream)
+    fa_bwd(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal,
+           scale, dq_mode, work.ws, stream)
+    fa_bwd_dq_finalize(work.dq_acc, dq, scale, stream)
+    return dq, dk, dv

@@ -1,0 +1,288 @@
+// C-ABI layer of libfabwd.so: argument checks, TMA descriptor encoding and
+// kernel launches.  Declarations and their contracts are in include/fabwd.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/fabwd.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_err[0] = '\0';
+  return FA_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks host offsets: batch+1 entries, cu[0] = 0, non-decreasing,
+// cu[batch] <= total.  Reports the longest sequence.
+int check_offsets(const int32_t* cu, int batch, int total, const char* name, int* max_len) {
+  if (cu == nullptr) return fail(FA_ERR_INVALID_ARG, "%s_host is NULL", name);
+  if (cu[0] != 0) return fail(FA_ERR_INVALID_ARG, "%s_host[0] must be 0, got %d", name, cu[0]);
+  int mx = 0;
+  for (int b = 0; b < batch; ++b) {
+    const long long len = static_cast<long long>(cu[b + 1]) - cu[b];
+    if (len < 0)
+      return fail(FA_ERR_INVALID_ARG, "%s_host must be non-decreasing: entry %d is %d, entry %d is %d", name, b + 1,
+                  cu[b + 1], b, cu[b]);
+    if (len > mx) mx = static_cast<int>(len);
+  }
+  if (cu[batch] > total)
+    return fail(FA_ERR_INVALID_ARG, "%s_host[batch] = %d exceeds the tensor's %d rows", name, cu[batch], total);
+  *max_len = mx;
+  return FA_OK;
+}
+
+int check_shape(int batch, int total_q, int total_kv, int heads, int head_dim) {
+  if (batch < 0) return fail(FA_ERR_INVALID_ARG, "batch must be >= 0, got %d", batch);
+  if (heads < 1) return fail(FA_ERR_INVALID_ARG, "heads must be >= 1, got %d", heads);
+  if (total_q < 0 || total_kv < 0) return fail(FA_ERR_INVALID_ARG, "total_q and total_kv must be >= 0");
+  if (head_dim != 64 && head_dim != 128)
+    return fail(FA_ERR_UNSUPPORTED, "head_dim must be 64 or 128, got %d", head_dim);
+  if (static_cast<long long>(heads) * head_dim > 65535 * 64)
+    return fail(FA_ERR_UNSUPPORTED, "heads * head_dim too large for a 2-D tensor map");
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A [rows, heads*head_dim] bf16 view with 64 x 128 boxes and 128-byte
+// swizzle; rows past `rows` read as zero.
+int make_map(CUtensorMap* m, const void* base, int rows, int heads, int head_dim, const char* name) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * head_dim, static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * head_dim * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return FA_OK;
+}
+
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(FA_ERR_UNSUPPORTED, "this library is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_last_error(void) { return g_err; }
+
+int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
+                 const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
+                 const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int head_dim, int causal,
+                 float scale, fa_stream_t stream) {
+  int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
+  if (rc) return rc;
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  if (!isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  int max_q = 0, max_kv = 0;
+  if ((rc = check_offsets(cu_q_host, batch, total_q, "cu_q", &max_q))) return rc;
+  if ((rc = check_offsets(cu_kv_host, batch, total_kv, "cu_kv", &max_kv))) return rc;
+  if (batch == 0 || max_q == 0) return ok();
+  if (!q || !k || !v || !o || !m || !l || !cu_q_dev || !cu_kv_dev)
+    return fail(FA_ERR_INVALID_ARG, "a device pointer is NULL");
+  if ((rc = check_device())) return rc;
+  fa::FwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.m = m;
+  p.l = l;
+  p.cu_q = cu_q_dev;
+  p.cu_kv = cu_kv_dev;
+  p.heads = heads;
+  p.causal = causal;
+  p.scale = scale;
+  cudaError_t e = fa::launch_fwd_stats(p, head_dim, batch, (max_q + 63) / 64, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fwd_stats launch");
+  return ok();
+}
+
+int fa_bwd_preprocess(const fa_bf16* o, const fa_bf16* dout, float* D, float* dq_acc, int total_q, int heads,
+                      int head_dim, fa_stream_t stream) {
+  int rc = check_shape(0, total_q, 0, heads, head_dim);
+  if (rc) return rc;
+  if (total_q == 0) return ok();
+  if (!o || !dout || !D || !dq_acc) return fail(FA_ERR_INVALID_ARG, "a device pointer is NULL");
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dq_acc))
+    return fail(FA_ERR_INVALID_ARG, "o, dout and dq_acc must be 16-byte aligned");
+  if ((rc = check_device())) return rc;
+  cudaError_t e = fa::launch_preprocess(o, dout, D, dq_acc, static_cast<long long>(total_q) * heads, head_dim,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
+  return ok();
+}
+
+size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int heads,
+                             int head_dim, int causal, int dq_mode) {
+  (void)cu_kv_host;
+  (void)causal;
+  if (check_shape(batch, 0, 0, heads, head_dim)) return 0;
+  if (dq_mode == FA_DQ_ATOMIC) {
+    ok();
+    return 0;
+  }
+  if (dq_mode != FA_DQ_DETERMINISTIC) {
+    fail(FA_ERR_INVALID_ARG, "dq_mode must be 0 or 1, got %d", dq_mode);
+    return 0;
+  }
+  if (!cu_q_host) {
+    fail(FA_ERR_INVALID_ARG, "cu_q_host is NULL");
+    return 0;
+  }
+  int max_q = 0;
+  for (int b = 0; b < batch; ++b) max_q = cu_q_host[b + 1] - cu_q_host[b] > max_q ? cu_q_host[b + 1] - cu_q_host[b] : max_q;
+  ok();
+  // one int32 ticket per (batch, head, 128-row query block), rounded to 256 B
+  const size_t n = static_cast<size_t>(batch) * heads * ((max_q + 127) / 128);
+  return ((n * 4 + 255) / 256) * 256;
+}
+
+int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m, const float* l,
+           const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+           const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads,
+           int head_dim, int causal, float scale, int dq_mode, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream) {
+  int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
+  if (rc) return rc;
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  if (dq_mode != FA_DQ_ATOMIC && dq_mode != FA_DQ_DETERMINISTIC)
+    return fail(FA_ERR_INVALID_ARG, "dq_mode must be 0 or 1, got %d", dq_mode);
+  if (dq_mode == FA_DQ_DETERMINISTIC) return fail(FA_ERR_UNSUPPORTED, "FA_DQ_DETERMINISTIC is not available yet");
+  if (!isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  int max_q = 0, max_kv = 0;
+  if ((rc = check_offsets(cu_q_host, batch, total_q, "cu_q", &max_q))) return rc;
+  if ((rc = check_offsets(cu_kv_host, batch, total_kv, "cu_kv", &max_kv))) return rc;
+  const int kv_used = batch > 0 ? cu_kv_host[batch] : 0;
+  const bool has_work = batch > 0 && max_kv > 0;
+  if (!has_work && total_kv == kv_used) return ok();
+  if ((total_kv > 0 && (!dk || !dv)) ||
+      (has_work && (!k || !v || !cu_q_dev || !cu_kv_dev)) ||
+      (has_work && max_q > 0 && (!q || !dout || !m || !l || !D || !dq_acc)))
+    return fail(FA_ERR_INVALID_ARG, "a device pointer is NULL");
+  const void* al[] = {q, k, v, dout, dq_acc, dk, dv};
+  for (const void* ptr : al)
+    if (ptr && !aligned16(ptr)) return fail(FA_ERR_INVALID_ARG, "q, k, v, dout, dq_acc, dk, dv must be 16-byte aligned");
+  const size_t need = fa_bwd_workspace_size(cu_q_host, cu_kv_host, batch, heads, head_dim, causal, dq_mode);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+    return fail(FA_ERR_INVALID_ARG, "workspace of %zu bytes needed, got %zu", need, workspace_bytes);
+  if ((rc = check_device())) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (total_kv > kv_used) {
+    const long long row_bytes = static_cast<long long>(heads) * head_dim * 2;
+    cudaError_t e = fa::launch_zero_fill(dk + static_cast<long long>(kv_used) * heads * head_dim,
+                                         (total_kv - kv_used) * row_bytes, s);
+    if (e == cudaSuccess)
+      e = fa::launch_zero_fill(dv + static_cast<long long>(kv_used) * heads * head_dim,
+                               (total_kv - kv_used) * row_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "padding zero fill");
+  }
+  if (!has_work) return ok();
+  fa::BwdParams p;
+  memset(&p, 0, sizeof(p));
+  // With no query rows at all no query tile is ever loaded; the key tensor
+  // then stands in as a valid address for the (unused) query maps.
+  const void* qbase = max_q > 0 ? static_cast<const void*>(q) : static_cast<const void*>(k);
+  const void* dobase = max_q > 0 ? static_cast<const void*>(dout) : static_cast<const void*>(k);
+  if ((rc = make_map(&p.tm_q, qbase, max_q > 0 ? total_q : total_kv, heads, head_dim, "q"))) return rc;
+  if ((rc = make_map(&p.tm_k, k, total_kv, heads, head_dim, "k"))) return rc;
+  if ((rc = make_map(&p.tm_v, v, total_kv, heads, head_dim, "v"))) return rc;
+  if ((rc = make_map(&p.tm_do, dobase, max_q > 0 ? total_q : total_kv, heads, head_dim, "dout"))) return rc;
+  p.m = m;
+  p.l = l;
+  p.D = D;
+  p.dq_acc = dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  p.cu_q = cu_q_dev;
+  p.cu_kv = cu_kv_dev;
+  p.heads = heads;
+  p.causal = causal;
+  p.dq_mode = dq_mode;
+  p.max_q_blocks = (max_q + 127) / 128;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.tickets = static_cast<int*>(workspace);
+  if (dq_mode == FA_DQ_DETERMINISTIC) {
+    cudaError_t e = fa::launch_zero_fill(workspace, static_cast<long long>(need), s);
+    if (e != cudaSuccess) return cuda_fail(e, "ticket reset");
+  }
+  cudaError_t e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, s);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
+  return ok();
+}
+
+int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads, int head_dim, float scale,
+                       fa_stream_t stream) {
+  int rc = check_shape(0, total_q, 0, heads, head_dim);
+  if (rc) return rc;
+  if (total_q == 0) return ok();
+  if (!dq_acc || !dq) return fail(FA_ERR_INVALID_ARG, "a device pointer is NULL");
+  if (!aligned16(dq_acc) || !aligned16(dq)) return fail(FA_ERR_INVALID_ARG, "dq_acc and dq must be 16-byte aligned");
+  if (!isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  if ((rc = check_device())) return rc;
+  cudaError_t e = fa::launch_dq_finalize(dq_acc, dq, static_cast<long long>(total_q) * heads * head_dim, scale,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  return ok();
+}
+
+int fa_check_device_status(fa_stream_t stream) {
+  int st = 0;
+  int e = fa::bwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "fa_check_device_status");
+  if (st == 4) return fail(FA_ERR_TIMEOUT, "a device-side wait in fa_bwd ran out of time (status %d)", st);
+  if (st != 0) return fail(FA_ERR_CUDA, "fa_bwd recorded device status %d", st);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,502 @@
+// Single-pass flash-attention backward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes follows the SK-16 single-pass FA Grad article: section 3
+// (skeleton C1 -> V1 -> C2 -> V2), section 3.1 (the eight per-block steps),
+// section 4.1 (m and l are consumed, never recomputed) and section 4.2
+// (bf16 operands, fp32 scores/softmax, P and dS rounded to bf16 before the
+// second group of matmuls, fp32 accumulation of dK, dV, dQ).  The loop order
+// is the key-block-outer one that section 1 names as best for dK/dV: a CTA
+// owns one (sequence, head, 128-row key block), keeps dK and dV in tensor
+// memory across its whole query sweep and adds each dQ partial into an
+// fp32 accumulator (section 3, V2 atomic write-back, restricted to dQ).
+//
+// Per query block i (128 rows), with the key block j fixed (128 rows):
+//   C1   S^T  = K_j Q_i^T              (TMEM cols [0,128), fp32)
+//        dP^T = V_j dO_i^T             (TMEM cols [128,256))
+//   V1   P    = exp2(S*scale*log2e - (m*log2e + log2 l))  (= exp(S*scale-m)/l)
+//        dS   = P * (dP - D)           masked entries exactly 0
+//        P  -> bf16 into TMEM cols [0,32) and [64,96) (A operand of dV)
+//        dS -> bf16 into shared memory (operand of dK and dQ)
+//   C2   dV_j += P^T dO_i              (TMEM cols [256, 256+d))
+//        dK_j += dS^T Q_i              (TMEM cols [256+d, 256+2d))
+//        dQ partial = dS K_j           (reuses TMEM cols [128,256))
+//   V2   dq_acc[rows of i] += partial  (fp32 atomics; scale applied later)
+// Transposed scores put key rows on TMEM lanes, so the softmax threads own
+// whole key rows and P / dS come out already in the layouts the C2 MMAs
+// want.  For d = 128 the dQ partial is produced transposed (d on lanes) so
+// that the atomic write-back of each warp covers 128 contiguous bytes.
+//
+// Warp roles (512 threads):
+//   warp 0      TMA producer: K, V once; Q, dO and per-row stats per block
+//               (2-stage ring); zeroes rows past a sequence end
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 4-11  two softmax warpgroups, each owning 64 of the 128 query
+//               columns for all 128 key rows; at the end dV (4-7), dK (8-11)
+//   warps 12-15 dQ write-back
+// Every mbarrier wait is bounded (see sm103.cuh); on a timeout the CTA
+// records FA_ERR_TIMEOUT in the status word, drains and frees TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+
+__device__ int g_bwd_status = 0;
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int BM = 128;   // key rows per CTA
+constexpr int BN = 128;   // query rows per block
+constexpr uint32_t CHUNK = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0;
+constexpr uint32_t COL_DP = 128;
+constexpr uint32_t COL_DV = 256;
+
+// mbarrier slots
+enum {
+  B_KV_FULL = 0, B_KV_READY, B_Q_FULL0, B_Q_FULL1, B_Q_READY0, B_Q_READY1, B_Q_EMPTY0, B_Q_EMPTY1,
+  B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_EMPTY, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
+  B_TEARDOWN, NUM_BARS
+};
+
+template <int D>
+struct Layout {
+  static constexpr uint32_t TILE = 128 * D * 2;   // [128 rows, D] bf16
+  static constexpr int NCH = D / 64;              // 64-column chunks per tile
+  static constexpr uint32_t K = 0;
+  static constexpr uint32_t V = TILE;
+  static constexpr uint32_t Q = 2 * TILE;         // 2 stages
+  static constexpr uint32_t DO = 4 * TILE;        // 2 stages
+  static constexpr uint32_t DS = 6 * TILE;        // [128 key rows, 128 query cols] bf16 = 32 KB
+  static constexpr uint32_t STATS = DS + 32768;   // per stage: lse2[128], D[128] (fp32)
+  static constexpr uint32_t BARS = STATS + 2 * 2 * 128 * 4;
+  static constexpr uint32_t MISC = BARS + NUM_BARS * 8;   // abort flag, TMEM address
+  static constexpr uint32_t BYTES = MISC + 16;
+  static constexpr uint32_t COL_DK = COL_DV + D;
+};
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int t) {
+  // 16-element K step t inside a [rows, K] tile stored as 64-column chunks
+  return sw128_desc(tile + (t >> 2) * CHUNK + (t & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int t) {
+  // rows 16t..16t+15 of a [K rows, MN] tile; MN chunks of 64 are CHUNK apart
+  return sw128_desc(tile + t * 2048, CHUNK, 1024);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Zero rows [first, 128) of a [128, D] tile (all chunks) with the 32 lanes
+// of one warp.  Each row of a chunk is one contiguous 128-byte line.
+template <int D>
+__device__ __forceinline__ void zero_rows(uint32_t tile, int first, int lane) {
+  constexpr int NCH = D / 64;
+  const int nrows = 128 - first;
+  for (int e = lane; e < nrows * NCH * 8; e += 32) {
+    const int row = first + e / (NCH * 8);
+    const int rem = e % (NCH * 8);
+    const int ch = rem / 8, g = rem % 8;
+    st_shared_v4(tile + ch * CHUNK + row * 128 + g * 16, 0u, 0u, 0u, 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int kvb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int H = p.heads;
+  const int q_start = p.cu_q[b], s1 = p.cu_q[b + 1] - q_start;
+  const int kv_start = p.cu_kv[b], s2 = p.cu_kv[b + 1] - kv_start;
+  if (kvb * BM >= s2) return;                       // CTA-uniform, before any barrier
+  if (sbase & 1023) {                               // swizzled tiles need 1 KB alignment
+    if (threadIdx.x == 0) atomicCAS(&g_bwd_status, 0, 99);
+    return;
+  }
+  const int kv_valid = min(BM, s2 - kvb * BM);
+  const int n_qb = (s1 + BN - 1) / BN;
+  const int qb0 = p.causal ? kvb : 0;               // top-left mask: query block >= key block
+  const int n_it = max(0, n_qb - qb0);
+  const long long rs = static_cast<long long>(H) * D;   // row stride (elements)
+
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC + 4);
+  const uint32_t bars = sbase + L::BARS;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  float* st_lse = reinterpret_cast<float*>(smem + L::STATS);          // [2][128]
+  float* st_D = reinterpret_cast<float*>(smem + L::STATS + 1024);     // [2][128]
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    mbar_init(bar(B_KV_FULL), 1);
+    mbar_init(bar(B_KV_READY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_Q_FULL0 + s), 1);
+      mbar_init(bar(B_Q_READY0 + s), 1);
+      mbar_init(bar(B_Q_EMPTY0 + s), 1);
+    }
+    mbar_init(bar(B_S_FULL), 1);
+    mbar_init(bar(B_DP_FULL), 1);
+    mbar_init(bar(B_P_READY), 256);
+    mbar_init(bar(B_P_USED), 1);
+    mbar_init(bar(B_DS_READY), 256);
+    mbar_init(bar(B_DS_EMPTY), 1);
+    mbar_init(bar(B_DQ_FULL), 1);
+    mbar_init(bar(B_DQ_EMPTY), 128);
+    mbar_init(bar(B_ACC_FULL), 1);
+    mbar_init(bar(B_TEARDOWN), 1);
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int* status = &g_bwd_status;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (n_it > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_do);
+        mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * L::TILE);
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_2d(sbase + L::K + c * CHUNK, &p.tm_k, h * D + c * 64, kv_start + kvb * BM, bar(B_KV_FULL));
+          tma_load_2d(sbase + L::V + c * CHUNK, &p.tm_v, h * D + c * 64, kv_start + kvb * BM, bar(B_KV_FULL));
+        }
+      }
+      __syncwarp();
+      // Loads issued but not yet seen complete must land before the CTA
+      // exits, even on the abort path: remember the barrier and its parity.
+      int pend_bar = B_KV_FULL;
+      uint32_t pend_par = 0;
+      bool ok = mbar_wait(bar(B_KV_FULL), 0, abort, status);
+      if (ok) {
+        pend_bar = -1;
+        if (kv_valid < BM) {
+          zero_rows<D>(sbase + L::K, kv_valid, lane);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_KV_READY));
+      }
+      for (int k = 0; ok && k < n_it; ++k) {
+        const int s = k & 1;
+        const int qb = qb0 + k;
+        const int q_row0 = q_start + qb * BN;
+        const int q_valid = min(BN, s1 - qb * BN);
+        if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), ((k >> 1) - 1) & 1, abort, status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), 2 * L::TILE);
+          for (int c = 0; c < L::NCH; ++c) {
+            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, h * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
+            tma_load_2d(sbase + L::DO + s * L::TILE + c * CHUNK, &p.tm_do, h * D + c * 64, q_row0,
+                        bar(B_Q_FULL0 + s));
+          }
+        }
+        pend_bar = B_Q_FULL0 + s;
+        pend_par = (k >> 1) & 1;
+        // Row statistics: lse2 = m*log2(e) + log2(l), and D.
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;
+          float lse2 = 0.f, dd = 0.f;
+          if (r < q_valid) {
+            const long long idx = static_cast<long long>(q_row0 + r) * H + h;
+            lse2 = p.m[idx] * 1.4426950408889634f + __log2f(p.l[idx]);
+            dd = p.D[idx];
+          }
+          st_lse[s * 128 + r] = lse2;
+          st_D[s * 128 + r] = dd;
+        }
+        if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;
+        pend_bar = -1;
+        if (q_valid < BN) {
+          zero_rows<D>(sbase + L::Q + s * L::TILE, q_valid, lane);
+          zero_rows<D>(sbase + L::DO + s * L::TILE, q_valid, lane);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
+      }
+      if (pend_bar >= 0) {
+        volatile int no_abort = 0;
+        mbar_wait(bar(pend_bar), pend_par, &no_abort, status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (n_it > 0 && lane == 0) {
+      constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);     // S^T, dP^T: K-major x K-major
+      constexpr uint32_t ID_KV = idesc_bf16(128, D, 0, 1);      // dV, dK: B (dO / Q) MN-major
+      constexpr uint32_t ID_DQ = (D == 128) ? idesc_bf16(128, 128, 1, 1)   // dQ^T = K^T dS^T
+                                            : idesc_bf16(128, 64, 1, 1);   // dQ = dS K
+      const uint32_t t_s = tmem + COL_S, t_dp = tmem + COL_DP;
+      const uint32_t t_dv = tmem + COL_DV, t_dk = tmem + L::COL_DK;
+      const uint32_t sK = sbase + L::K, sV = sbase + L::V, sDS = sbase + L::DS;
+      bool ok = mbar_wait(bar(B_KV_READY), 0, abort, status);
+      for (int k = 0; ok && k < n_it; ++k) {
+        const int s = k & 1;
+        const uint32_t ph = k & 1;
+        const uint32_t sQ = sbase + L::Q + s * L::TILE, sDO = sbase + L::DO + s * L::TILE;
+        if (!mbar_wait(bar(B_Q_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
+        // P of the previous block (read by its dV MMAs) lives in the S columns.
+        if (k > 0 && !mbar_wait(bar(B_P_USED), (k - 1) & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < D / 16; ++t) mma_ss(t_s, desc_kmajor(sK, t), desc_kmajor(sQ, t), ID_S, t > 0);
+        mma_commit(bar(B_S_FULL));
+        // The previous dQ partial occupies the dP columns until written back.
+        if (k > 0 && !mbar_wait(bar(B_DQ_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < D / 16; ++t) mma_ss(t_dp, desc_kmajor(sV, t), desc_kmajor(sDO, t), ID_S, t > 0);
+        mma_commit(bar(B_DP_FULL));
+        // dV += P^T dO with P (bf16) read from TMEM.
+        if (!mbar_wait(bar(B_P_READY), ph, abort, status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < BN / 16; ++t)   // P of query rows 16t.. sits at column 64*(t/4) + 8*(t%4)
+          mma_ts(t_dv, t_s + (t >> 2) * 64 + (t & 3) * 8, desc_mnmajor(sDO, t), ID_KV, (k > 0 || t > 0));
+        mma_commit(bar(B_P_USED));
+        // dK += dS^T Q and the dQ partial, both from dS in shared memory.
+        if (!mbar_wait(bar(B_DS_READY), ph, abort, status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < BN / 16; ++t)
+          mma_ss(t_dk, desc_kmajor(sDS, t), desc_mnmajor(sQ, t), ID_KV, (k > 0 || t > 0));
+        if (D == 128) {
+#pragma unroll
+          for (int t = 0; t < BM / 16; ++t) mma_ss(t_dp, desc_mnmajor(sK, t), desc_mnmajor(sDS, t), ID_DQ, t > 0);
+        } else {
+#pragma unroll
+          for (int t = 0; t < BM / 16; ++t) mma_ss(t_dp, desc_mnmajor(sDS, t), desc_mnmajor(sK, t), ID_DQ, t > 0);
+        }
+        mma_commit(bar(B_DS_EMPTY));
+        mma_commit(bar(B_DQ_FULL));
+        mma_commit(bar(B_Q_EMPTY0 + s));
+      }
+      if (ok) {
+        mma_commit(bar(B_ACC_FULL));
+      } else {
+        // Aborted: wait (bounded) for every MMA issued so far before TMEM is freed.
+        mma_commit(bar(B_TEARDOWN));
+        volatile int no_abort = 0;
+        mbar_wait(bar(B_TEARDOWN), 0, &no_abort, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ softmax / dS
+    const int wg = (warp - 4) >> 2;          // 0: query columns 0-63, 1: 64-127
+    const int quarter = warp & 3;            // TMEM lane quarter
+    const int r = quarter * 32 + lane;       // key row within the block
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int k = 0; k < n_it; ++k) {
+      const int s = k & 1;
+      const uint32_t ph = k & 1;
+      const int qb = qb0 + k;
+      const int q_valid = min(BN, s1 - qb * BN);
+      const bool diag = p.causal && (qb == kvb);
+      const bool need_mask = diag || q_valid < BN || kv_valid < BM;
+      // query index - key index threshold for the top-left causal mask: column c
+      // (global within block) is visible from row r iff c >= r when qb == kvb.
+      if (!mbar_wait(bar(B_Q_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
+      if (!mbar_wait(bar(B_S_FULL), ph, abort, status)) { ok = false; break; }
+      tc_fence_after();
+      const float* lse = st_lse + s * 128 + wg * 64;
+      const float* dvec = st_D + s * 128 + wg * 64;
+      float P[64];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_addr + COL_S + wg * 64 + half * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int col = half * 32 + c;          // within this warpgroup's 64 columns
+          float pv = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -lse[col]));
+          if (need_mask) {
+            const int qc = wg * 64 + col;
+            const bool vis = (r < kv_valid) && (qc < q_valid) && (!diag || qc >= r);
+            pv = vis ? pv : 0.f;
+          }
+          P[col] = pv;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(P[half * 32 + 2 * j], P[half * 32 + 2 * j + 1]);
+        // P goes into columns this warpgroup has already read (the other
+        // warpgroup may still be reading its own half of S).
+        tmem_st16(tmem + lane_addr + COL_S + wg * 64 + half * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_READY));
+
+      if (!mbar_wait(bar(B_DP_FULL), ph, abort, status)) { ok = false; break; }
+      if (k > 0 && !mbar_wait(bar(B_DS_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t ds_row = sbase + L::DS + wg * CHUNK + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_addr + COL_DP + wg * 64 + half * 32, v);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c0 = half * 32 + 2 * j;
+          float d0 = P[c0] * (__uint_as_float(v[2 * j]) - dvec[c0]);
+          float d1 = P[c0 + 1] * (__uint_as_float(v[2 * j + 1]) - dvec[c0 + 1]);
+          if (need_mask) {
+            // P is already 0 where masked, but dP may hold garbage there.
+            d0 = (P[c0] != 0.f) ? d0 : 0.f;
+            d1 = (P[c0 + 1] != 0.f) ? d1 : 0.f;
+          }
+          pk[j] = pack_bf16x2(d0, d1);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int gg = half * 4 + g;            // 16-byte granule within the 128-byte row
+          st_shared_v4(ds_row + ((gg ^ (r & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_DS_READY));
+    }
+    // ------------------------------------------------------------ dK / dV epilogue
+    const int kv_row = kv_start + kvb * BM + r;
+    uint16_t* out = (wg == 0) ? p.dv : p.dk;
+    const float mul = (wg == 0) ? 1.f : p.scale;
+    uint8_t* dst = reinterpret_cast<uint8_t*>(out + static_cast<long long>(kv_row) * rs + h * D);
+    if (n_it == 0) {
+      if (r < kv_valid)
+        for (int c = 0; c < D; c += 8) st_global_v4(dst + c * 2, 0u, 0u, 0u, 0u);
+    } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar(B_ACC_FULL), 0, abort, status))) {
+      tc_fence_after();
+      const uint32_t col0 = (wg == 0) ? COL_DV : L::COL_DK;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_addr + col0 + ch * 32, v);
+        tmem_ld_wait();
+        if (r < kv_valid) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              w[j] = pack_bf16x2(mul * __uint_as_float(v[8 * g + 2 * j]), mul * __uint_as_float(v[8 * g + 2 * j + 1]));
+            st_global_v4(dst + (ch * 32 + g * 8) * 2, w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ write-back
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane;       // TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    for (int k = 0; k < n_it; ++k) {
+      const int qb = qb0 + k;
+      const int q_valid = min(BN, s1 - qb * BN);
+      const long long q_row0 = q_start + qb * BN;
+      if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
+      tc_fence_after();
+      if (D == 128) {
+        // lanes = head-dim index t, columns = query rows
+        float* base = p.dq_acc + q_row0 * rs + h * D + t;
+#pragma unroll
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + COL_DP + ch * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int q = ch * 32 + c;
+            if (q < q_valid) atomicAdd(base + q * rs, __uint_as_float(v[c]));
+          }
+        }
+      } else {
+        // lanes = query rows, columns = head-dim index
+        float* base = p.dq_acc + (q_row0 + t) * rs + h * D;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + COL_DP + ch * 32, v);
+          tmem_ld_wait();
+          if (t < q_valid) {
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              atomicAdd(reinterpret_cast<float4*>(base + ch * 32 + c4 * 4),
+                        make_float4(__uint_as_float(v[4 * c4]), __uint_as_float(v[4 * c4 + 1]),
+                                    __uint_as_float(v[4 * c4 + 2]), __uint_as_float(v[4 * c4 + 3])));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_DQ_EMPTY));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const BwdParams& p, int batch, int max_kv_blocks, cudaStream_t s) {
+  constexpr uint32_t bytes = Layout<D>::BYTES;
+  static_assert(bytes <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(max_kv_blocks, p.heads, batch);
+  bwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, cudaStream_t s) {
+  if (batch <= 0 || max_kv_blocks <= 0) return cudaSuccess;
+  return head_dim == 64 ? launch_d<64>(p, batch, max_kv_blocks, s) : launch_d<128>(p, batch, max_kv_blocks, s);
+}
+
+int bwd_read_and_clear_status(cudaStream_t s, int* status) {
+  int zero = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  e = cudaMemcpyFromSymbol(status, g_bwd_status, sizeof(int));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  e = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int));
+  return static_cast<int>(e);
+}
+
+}  // namespace fa

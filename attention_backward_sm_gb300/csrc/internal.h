@@ -1,0 +1,59 @@
+// Launch interfaces shared between the C-ABI layer (api.cu) and the kernel
+// translation units.  Host-only declarations; no kernel code here.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Everything the single-pass backward kernel needs, passed by value as one
+// __grid_constant__ parameter (the tensor maps must live in parameter
+// space for TMA).
+struct BwdParams {
+  CUtensorMap tm_q;   // [total_q rows, H*d cols] bf16, box 64 x 128, 128B swizzle
+  CUtensorMap tm_k;   // [total_kv rows, H*d cols]
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;  // [total_q rows, H*d cols]
+  const float* m;
+  const float* l;
+  const float* D;
+  float* dq_acc;
+  uint16_t* dk;
+  uint16_t* dv;
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  int* tickets;        // deterministic mode: one counter per (batch, head, query block)
+  int heads;
+  int causal;
+  int dq_mode;
+  int max_q_blocks;    // query blocks of the longest query sequence
+  float scale;         // softmax scale (multiplies dK in the epilogue)
+  float scale_log2;    // scale * log2(e)
+};
+
+cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, cudaStream_t s);
+int bwd_read_and_clear_status(cudaStream_t s, int* status);
+
+cudaError_t launch_preprocess(const uint16_t* o, const uint16_t* dout, float* D, float* dq_acc, long long rows,
+                              int head_dim, cudaStream_t s);
+cudaError_t launch_dq_finalize(const float* acc, uint16_t* dq, long long elems, float scale, cudaStream_t s);
+cudaError_t launch_zero_fill(void* p, long long bytes, cudaStream_t s);
+
+struct FwdParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  uint16_t* o;
+  float* m;
+  float* l;
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  int heads;
+  int causal;
+  float scale;
+};
+cudaError_t launch_fwd_stats(const FwdParams& p, int head_dim, int batch, int max_q_blocks64, cudaStream_t s);
+
+}  // namespace fa

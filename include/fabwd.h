@@ -1,0 +1,132 @@
+/*
+ * fabwd.h -- C ABI of libfabwd.so, a single-pass flash-attention backward
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (cited by page title and section):
+ *   "PyPTO-Gym SK-16: single-pass Attention backward (FA Grad)" article,
+ *   section 3 (kernel skeleton with inputs q, k, v, o, do, l, m and outputs
+ *   dq, dk, dv over packed variable-length batches with cumulative offsets
+ *   actual_q / actual_kv), section 3.1 (the eight per-block steps) and
+ *   section 4.2 (dtype table).  For each sequence b and head h, with
+ *   X = scale * Q K^T (masked entries -inf):
+ *       P  = exp(X - m) / l              (m, l given, never recomputed)
+ *       dP = dO V^T,  D = rowsum(O * dO), dS = P * (dP - D)
+ *       dV = P^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K
+ *   The causal mask is top-left aligned (key j visible to query i iff
+ *   j <= i, local indices; the JAX cuDNN wrapper's MaskType.CAUSAL).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are packed and contiguous.  q, o, dout, dq: [total_q, H, d];
+ *     k, v, dk, dv: [total_kv, H, d]; m, l, D: [total_q, H] (float32).
+ *     Element type fa_bf16 is the raw 16-bit pattern of a bfloat16.
+ *     The head h of row r sits at element offset (r * H + h) * d.
+ *   - cu_q / cu_kv are int32 cumulative offsets with batch+1 entries,
+ *     cu[0] = 0, non-decreasing, cu[batch] <= total.  Sequence b owns
+ *     rows [cu[b], cu[b+1]).  Rows at or beyond cu[batch] are padding.
+ *     Entry points that take both a device and a host copy need both to
+ *     hold the same values: the host copy sizes the launch.
+ *   - All device pointers are caller-owned device memory, 16-byte aligned.
+ *     The library allocates no device memory on these paths.
+ *   - head_dim must be 64 or 128; heads >= 1.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
+ *     default stream) and returns FA_OK or an error code.  Arguments are
+ *     checked on the host before anything is launched; on an error nothing
+ *     is launched and fa_last_error() describes the problem.
+ *   - Device-side waits are bounded.  A kernel whose internal wait runs out
+ *     records FA_ERR_TIMEOUT in a device status word and returns early;
+ *     fa_check_device_status() reads and clears it.
+ */
+#ifndef FABWD_H
+#define FABWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t fa_bf16;               /* bfloat16 bit pattern */
+typedef struct CUstream_st* fa_stream_t;  /* same type as cudaStream_t */
+
+enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null pointer, bad offsets, bad sizes, misalignment */
+    FA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, no sm_103a device */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+    FA_ERR_TIMEOUT = 4        /* a device-side bounded wait ran out */
+};
+
+enum fa_dq_mode {
+    FA_DQ_ATOMIC = 0,         /* dQ partials added with fp32 atomics, in any order */
+    FA_DQ_DETERMINISTIC = 1   /* dQ partials added in ascending key-block order: bitwise reproducible */
+};
+
+/* Forward statistics used to build consistent backward inputs (support
+ * step; the SK-16 article, section 5, says the forward skeleton supplies
+ * l and m).  Writes O = softmax(scale*QK^T) V (bf16), m_i = max_j of the
+ * scaled scores and l_i = sum_j exp(scaled score - m_i) (float32) for every
+ * row of every sequence.  Rows of a sequence with no keys get O = 0,
+ * m = -inf, l = 0.  Padding rows are not written. */
+int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
+                 fa_bf16* o, float* m, float* l,
+                 const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+                 const int32_t* cu_q_host, const int32_t* cu_kv_host,
+                 int batch, int total_q, int total_kv, int heads, int head_dim,
+                 int causal, float scale, fa_stream_t stream);
+
+/* Backward preprocess (section 3.1 step 4; section 4.2 row "D"):
+ * D[r, h] = sum_k float(O[r,h,k]) * float(dO[r,h,k]) for every row
+ * r < total_q, and dq_acc[r, h, :] = 0 (float32 accumulator of
+ * [total_q, H, d]; the SK-16 host pre-zeroes its atomic targets, section 4).
+ */
+int fa_bwd_preprocess(const fa_bf16* o, const fa_bf16* dout, float* D, float* dq_acc,
+                      int total_q, int heads, int head_dim, fa_stream_t stream);
+
+/* Bytes of device workspace fa_bwd needs for these shapes and dq_mode
+ * (0 for FA_DQ_ATOMIC).  Returns 0 and sets fa_last_error() on bad
+ * arguments, so check fa_last_error() when a mode needs workspace. */
+size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host,
+                             int batch, int heads, int head_dim, int causal, int dq_mode);
+
+/* The single-pass backward (section 3: C1 -> V1 -> C2 -> V2), key-block
+ * outer.  Each CTA owns one (sequence, head, 128-row key block), keeps
+ * its dK and dV accumulators in tensor memory for the whole query sweep and
+ * writes them once; the unscaled dS K partial of every (query block, key
+ * block) pair is added into dq_acc (float32, zeroed by fa_bwd_preprocess).
+ * Inputs: q, k, v, dout (bf16), m, l (the forward statistics, consumed as
+ * given: section 4.1) and D from fa_bwd_preprocess.  Outputs: dk = bf16(scale
+ * * dS^T Q) and dv = bf16(P^T dO) for every key row of every sequence
+ * (exact zeros for keys no query sees), zeros in padding rows
+ * [cu_kv[batch], total_kv).  dq_acc must then go through
+ * fa_bwd_dq_finalize.  workspace: at least fa_bwd_workspace_size() bytes
+ * (may be NULL when that is 0); its contents need no initialisation. */
+int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout,
+           const float* m, const float* l, const float* D,
+           float* dq_acc, fa_bf16* dk, fa_bf16* dv,
+           const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+           const int32_t* cu_q_host, const int32_t* cu_kv_host,
+           int batch, int total_q, int total_kv, int heads, int head_dim,
+           int causal, float scale, int dq_mode,
+           void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* dQ write-back (section 3, V2 applies scale to dq; section 4.2 row dQ:
+ * fp32 accumulate, then bf16): dq[e] = bf16_rne(scale * dq_acc[e]) for all
+ * total_q * heads * head_dim elements. */
+int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads,
+                       int head_dim, float scale, fa_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word
+ * that bounded waits set.  Returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_CUDA. */
+int fa_check_device_status(fa_stream_t stream);
+
+/* Message describing the last error returned on the calling thread
+ * (empty string after success).  The pointer stays valid until the next
+ * call on the same thread. */
+const char* fa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FABWD_H */

@@ -1,0 +1,114 @@
+"""Shared helpers of the GPU parity tests: inputs, oracle references and the
+comparison rule.
+
+The rule for every gradient (the target specification): relative L2 error
+<= 1e-2 and max |error| <= 3e-2 * max |reference| against the fp64 oracle,
+and the GPU value exactly 0 wherever the oracle is exactly 0 (padding rows,
+keys no query sees).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import seeded_inputs as si
+
+REL_L2 = 1e-2
+MAX_ABS = 3e-2
+
+
+def compare(name, got, ref, exact_zero_mask=None):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    nref = np.linalg.norm(ref)
+    if nref == 0:
+        assert np.all(got == 0), f"{name}: reference is all zero, GPU is not"
+        return 0.0
+    rel = np.linalg.norm(got - ref) / nref
+    mx = np.abs(got - ref).max()
+    assert rel <= REL_L2, f"{name}: relative L2 error {rel:.3e} > {REL_L2}"
+    assert mx <= MAX_ABS * np.abs(ref).max(), f"{name}: max abs error {mx:.3e} > {MAX_ABS} * {np.abs(ref).max():.3e}"
+    zmask = (ref == 0) if exact_zero_mask is None else exact_zero_mask
+    bad = np.count_nonzero(got[zmask] != 0)
+    assert bad == 0, f"{name}: {bad} non-zero values where the result must be exactly 0"
+    return rel
+
+
+def to_np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+class Prepared:
+    """Device copies of one case's inputs with O, m, l for the checked heads
+    taken from the oracle forward (rounded to bf16 / fp32).  Heads that are
+    not checked use the library's forward statistics."""
+
+    def __init__(self, case: si.Case, heads_subset=None, device="cuda"):
+        import attention_backward_sm_gb300 as fab
+        self.case = case
+        self.heads_subset = heads_subset
+        q, k, v, do = case.tensors()
+        self.cpu = (q, k, v, do)
+        self.scale = case.softmax_scale
+        dev = torch.device(device)
+        self.cu_q = torch.from_numpy(case.cu_q).to(dev)
+        self.cu_kv = torch.from_numpy(case.cu_kv).to(dev)
+        self.q, self.k, self.v, self.do = (t.to(dev) for t in (q, k, v, do))
+        o64, m64, l64 = oracle.forward_packed(q, k, v, case.cu_q, case.cu_kv, self.scale, case.causal,
+                                              heads_subset=heads_subset)
+        o = torch.from_numpy(o64).to(torch.bfloat16)
+        m = torch.from_numpy(m64).to(torch.float32)
+        l = torch.from_numpy(l64).to(torch.float32)
+        if heads_subset is None:
+            self.o, self.m, self.l = o.to(dev), m.to(dev), l.to(dev)
+        else:
+            self.o, self.m, self.l = fab.forward_stats(self.q, self.k, self.v, self.cu_q, self.cu_kv, case.cu_q,
+                                                       case.cu_kv, case.causal, self.scale)
+            for b, h in heads_subset:
+                rows = slice(int(case.cu_q[b]), int(case.cu_q[b + 1]))
+                self.o[rows, h] = o[rows, h].to(dev)
+                self.m[rows, h] = m[rows, h].to(dev)
+                self.l[rows, h] = l[rows, h].to(dev)
+        self.o_cpu = o
+        self.m_cpu = m
+        self.l_cpu = l
+
+    def reference(self):
+        q, k, v, do = self.cpu
+        return oracle.backward_packed(q, k, v, self.o_cpu, do, self.m_cpu, self.l_cpu, self.case.cu_q,
+                                      self.case.cu_kv, self.scale, self.case.causal,
+                                      heads_subset=self.heads_subset)
+
+    def run(self, dq_mode=0):
+        import attention_backward_sm_gb300 as fab
+        out = fab.backward(self.q, self.k, self.v, self.o, self.do, self.m, self.l, self.cu_q, self.cu_kv,
+                           self.case.cu_q, self.case.cu_kv, self.case.causal, self.scale, dq_mode)
+        torch.cuda.synchronize()
+        fab.fa_check_device_status()
+        return out
+
+
+def check_case(prep: Prepared, out=None, dq_mode=0):
+    """Compares the GPU gradients with the oracle on the checked heads."""
+    dq, dk, dv = out if out is not None else prep.run(dq_mode)
+    ref = prep.reference()
+    case = prep.case
+    units = prep.heads_subset or [(b, h) for b in range(case.batch) for h in range(case.heads)]
+    got = (to_np(dq), to_np(dk), to_np(dv))
+    errs = {}
+    if prep.heads_subset is None:
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref[:3]):
+            errs[name] = compare(name, g, r)
+    else:
+        for b, h in units:
+            qr = slice(int(case.cu_q[b]), int(case.cu_q[b + 1]))
+            kr = slice(int(case.cu_kv[b]), int(case.cu_kv[b + 1]))
+            for name, g, r, rows in zip(("dq", "dk", "dv"), got, ref[:3], (qr, kr, kr)):
+                errs[f"{name}[{b},{h}]"] = compare(f"{name}[b={b},h={h}]", g[rows, h], r[rows, h])
+    # padding rows past the last sequence are exactly zero for every head
+    nq, nkv = int(case.cu_q[-1]), int(case.cu_kv[-1])
+    assert np.all(got[0][nq:] == 0) and np.all(got[1][nkv:] == 0) and np.all(got[2][nkv:] == 0)
+    return errs

@@ -1,0 +1,84 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry
+point declared in include/fabwd.h; host-side argument checks return their
+error codes before anything touches the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "fabwd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_backward_sm_gb300 import build
+    build.build()
+    from attention_backward_sm_gb300 import _lib
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("fa_fwd_stats", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_dq_finalize", "fa_bwd_workspace_size",
+                 "fa_check_device_status", "fa_last_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from attention_backward_sm_gb300 import _lib
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def _offsets(*xs):
+    return np.asarray(xs, dtype=np.int32)
+
+
+def _call_bwd(lib, cu_q, cu_kv, heads=2, head_dim=128, causal=0, dq_mode=0, total_q=None, total_kv=None,
+              scale=0.1):
+    p = ctypes.c_void_p(16)   # never dereferenced: the checks fail first
+    total_q = int(cu_q[-1]) if total_q is None else total_q
+    total_kv = int(cu_kv[-1]) if total_kv is None else total_kv
+    return lib.fa_bwd(p, p, p, p, p, p, p, p, p, p, p, p, cu_q.ctypes.data_as(ctypes.c_void_p),
+                      cu_kv.ctypes.data_as(ctypes.c_void_p), len(cu_q) - 1, total_q, total_kv, heads, head_dim,
+                      causal, scale, dq_mode, None, 0, None)
+
+
+def test_host_argument_checks(lib):
+    cu = _offsets(0, 10, 30)
+    assert _call_bwd(lib, cu, cu, head_dim=96) == 2            # FA_ERR_UNSUPPORTED
+    assert b"head_dim" in lib.fa_last_error()
+    assert _call_bwd(lib, _offsets(0, 10, 5), cu) == 1         # decreasing offsets
+    assert b"non-decreasing" in lib.fa_last_error()
+    assert _call_bwd(lib, _offsets(1, 10, 30), cu) == 1        # cu[0] != 0
+    assert _call_bwd(lib, cu, cu, total_kv=20) == 1            # offsets exceed the tensor
+    assert _call_bwd(lib, cu, cu, heads=0) == 1
+    assert _call_bwd(lib, cu, cu, causal=2) == 1
+    assert _call_bwd(lib, cu, cu, dq_mode=7) == 1
+    assert _call_bwd(lib, cu, cu, scale=float("inf")) == 1
+    p = ctypes.c_void_p(16)
+    assert lib.fa_bwd_preprocess(p, p, p, p, 10, 2, 80, None) == 2
+    assert lib.fa_bwd_dq_finalize(p, p, 10, 0, 128, 1.0, None) == 1
+    # an empty problem is a successful no-op
+    z = _offsets(0)
+    assert _call_bwd(lib, z, z, total_q=0, total_kv=0) == 0
+    assert lib.fa_last_error() == b""
+
+
+def test_workspace_size(lib):
+    cu = _offsets(0, 300, 700)
+    hp = cu.ctypes.data_as(ctypes.c_void_p)
+    assert lib.fa_bwd_workspace_size(hp, hp, 2, 4, 128, 1, 0) == 0
+    n = lib.fa_bwd_workspace_size(hp, hp, 2, 4, 128, 1, 1)
+    assert n >= 2 * 4 * 4 * 4 and n % 256 == 0               # one int32 per (b, h, query block)
+    assert lib.fa_bwd_workspace_size(hp, hp, 2, 4, 128, 1, 5) == 0
+    assert b"dq_mode" in lib.fa_last_error()
