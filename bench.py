@@ -1,0 +1,405 @@
+"""Benchmark of the single-pass flash-attention backward on GB300.
+
+One step = the whole hot path on one batch: fa_bwd_preprocess (D and the
+zeroed dQ accumulator) -> fa_bwd (the tcgen05 kernel) -> fa_bwd_dq_finalize.
+Default workload: B=4, H=16, s1=s2=4096, head_dim=128, non-causal, the
+shape the throughput target is stated on.  FLOPs per step = 10*s1*s2*d*H*B
+(halved when causal).  Inputs are synthetic (seeded N(0,1) bf16); O, m, l
+come from the library's forward-statistics kernel before timing.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload cfg3nc|cfg2|...]
+  python bench.py --impl reference     # the fp64 CPU oracle on the same workload
+
+Under torchrun every rank runs its own copy of the workload (the path
+shards over independent (sequence, head) units with no collective: weak
+scaling); rank 0 prints one JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "FA-backward TFLOP/s (bf16, device-timed) and % of GB300 dense BF16 peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("bwd_main.cu", "sm103.cuh"):
+        with open(os.path.join(ROOT, "attention_backward_sm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per fa_bwd launch from the committed ncu summary, if it was
+    taken on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", f"fa_bwd_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    mh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_source_hash():
+        return None
+    return float(mt.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed
+    region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() in ("active", "0x1", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_case(name: str) -> si.Case:
+    return si.CONFIGS[name]()
+
+
+_TENSORS = {}
+
+
+def case_tensors(case: si.Case):
+    """CPU inputs of a case, generated once per process."""
+    if case.name not in _TENSORS:
+        _TENSORS[case.name] = case.tensors()
+    return _TENSORS[case.name]
+
+
+def workload_desc(case: si.Case) -> str:
+    if len(set(case.q_lens)) == 1 and len(set(case.kv_lens)) == 1:
+        return (f"B={case.batch} H={case.heads} s1={case.q_lens[0]} s2={case.kv_lens[0]} d={case.head_dim} "
+                f"{'causal' if case.causal else 'non-causal'}")
+    return (f"varlen B={case.batch} H={case.heads} d={case.head_dim} q_lens={case.q_lens} "
+            f"kv_lens={case.kv_lens} {'causal' if case.causal else 'non-causal'}")
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(case: si.Case, budget_s: float, max_units: int | None = None):
+    """Times the fp64 oracle backward on whole (sequence, head) units of the
+    workload until about budget_s seconds of CPU work.  Returns
+    (flops, seconds, units)."""
+    import oracle
+    q, k, v, do = case_tensors(case)
+    flops, secs, units = 0.0, 0.0, 0
+    order = [(b, h) for b in range(case.batch) for h in range(case.heads)]
+    for b, h in order:
+        qs, qe = int(case.cu_q[b]), int(case.cu_q[b + 1])
+        ks, ke = int(case.cu_kv[b]), int(case.cu_kv[b + 1])
+        qq, kk, vv, dd = q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], do[qs:qe, h]
+        o, m, l = oracle.forward_head(qq, kk, vv, case.softmax_scale, case.causal)   # inputs, untimed
+        t0 = time.perf_counter()
+        oracle.backward_head(qq, kk, vv, o, dd, m, l, case.softmax_scale, case.causal)
+        secs += time.perf_counter() - t0
+        f = 10.0 * (qe - qs) * (ke - ks) * case.head_dim
+        flops += f / 2 if case.causal else f
+        units += 1
+        if secs >= budget_s or (max_units and units >= max_units):
+            break
+    return flops, secs, units
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_rows(case: si.Case, rows: int, b: int = 0, h: int = 0):
+    """Times the fp64 oracle backward of the first `rows` query rows of one
+    (sequence, head) unit against all of its keys: dQ of those rows and
+    their share of dK and dV.  Returns (flops, seconds)."""
+    import oracle
+    q, k, v, do = case_tensors(case)
+    qs = int(case.cu_q[b])
+    ks, ke = int(case.cu_kv[b]), int(case.cu_kv[b + 1])
+    rows = max(1, min(rows, int(case.cu_q[b + 1]) - qs))
+    qq, kk, vv, dd = q[qs:qs + rows, h], k[ks:ke, h], v[ks:ke, h], do[qs:qs + rows, h]
+    o, m, l = oracle.forward_head(qq, kk, vv, case.softmax_scale, case.causal)   # inputs, untimed
+    t0 = time.perf_counter()
+    oracle.backward_head(qq, kk, vv, o, dd, m, l, case.softmax_scale, case.causal)
+    secs = time.perf_counter() - t0
+    s2 = ke - ks
+    if case.causal:
+        pairs = sum(min(i + 1, s2) for i in range(rows))
+    else:
+        pairs = rows * s2
+    return 10.0 * pairs * case.head_dim, secs
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    case = make_case(args.workload)
+    # Size each step's sample so that warm-up plus timed steps stay near
+    # three minutes of CPU time: calibrate on 256 query rows first.
+    f0, s0 = oracle_rows(case, 256)
+    rate = f0 / max(s0, 1e-9)
+    per_step_s = min(20.0, 180.0 / max(1, args.steps + args.warmup))
+    unit_pairs = case.q_lens[0] * case.kv_lens[0]
+    rows = int(max(64, min(case.q_lens[0], per_step_s * rate / (10.0 * case.head_dim * case.kv_lens[0]))))
+    for _ in range(args.warmup):
+        oracle_rows(case, rows)
+    total_f, total_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, s = oracle_rows(case, rows)
+        total_f += f
+        total_s += s
+    value = total_f / total_s / 1e12
+    sample = (f"fp64 backward of query rows [0, {rows}) of (sequence 0, head 0) against all "
+              f"{case.kv_lens[0]} keys per step ({total_f / args.steps:.3e} FLOP; a full unit has "
+              f"{unit_pairs} score entries)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {workload_desc(case)}", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import attention_backward_sm_gb300 as fab
+    from attention_backward_sm_gb300 import build as fab_build
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fab_build.build()
+    if pg is not None:
+        pg.barrier()
+    fab.lib()
+
+    case = make_case(args.workload)
+    q, k, v, do = (t.to(dev) for t in case_tensors(case))
+    cu_q = torch.from_numpy(case.cu_q).to(dev)
+    cu_kv = torch.from_numpy(case.cu_kv).to(dev)
+    scale = case.softmax_scale
+    o, m, l = fab.forward_stats(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale)
+    work = fab.Workspace(q, case.cu_q, case.cu_kv, case.causal, args.dq_mode)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    flops = case.flops()
+    launches_per_step = 3 + (1 if args.dq_mode == 1 else 0) + (2 if case.total_kv > int(case.cu_kv[-1]) else 0)
+    input_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do, o, m, l, work.dq_acc))
+
+    def step(ev=None):
+        fab.fa_bwd_preprocess(o, do, work.D, work.dq_acc)
+        if ev is not None:
+            ev[0].record(stream)
+        fab.fa_bwd(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q, cu_kv, case.cu_q, case.cu_kv,
+                   case.causal, scale, args.dq_mode, work.ws)
+        if ev is not None:
+            ev[1].record(stream)
+        fab.fa_bwd_dq_finalize(work.dq_acc, dq, scale)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    fab.fa_check_device_status()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg is not None:
+        pg.barrier()
+    clk = clocks.stop() if clocks else None
+    fab.fa_check_device_status()
+    elapsed_ms = start.elapsed_time(end)
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if pg is not None:
+        t = torch.tensor([elapsed_ms, bwd_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms, bwd_ms = float(t[0]), float(t[1])
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (q, k, v, o, do, m, l)]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+        dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, m, l)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for d_, h_ in zip(dev_in, host_in):
+                d_.copy_(h_, non_blocking=True)
+            outs = fab.backward(*dev_in, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, args.dq_mode,
+                                out=(dq, dk, dv), work=work)
+            for h_, d_ in zip(host_out, outs):
+                h_.copy_(d_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s2.elapsed_time(e2) / n_e2e
+        if pg is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+
+    peak, hbm, peak_src = peaks()
+    achieved = flops / (bwd_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "kernel": "fa_bwd (bwd_kernel<%d>)" % case.head_dim, "fa_bwd_ms": bwd_ms,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        f, s, u = oracle_sample(case, args.cpu_budget)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"fp64 backward of {u} (sequence, head) unit(s) of the workload, {f:.3e} FLOP in {s:.2f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {workload_desc(case)}", "dq_mode": args.dq_mode,
+                   "l2": f"inputs larger than L2 ({input_bytes / 2**20:.0f} MiB resident per step)"
+                   if input_bytes > L2_BYTES else "inputs smaller than L2",
+                   "flops_per_step": flops},
+        "frac_of_peak_step": value / world / peak,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="cfg3nc", choices=sorted(si.CONFIGS))
+    ap.add_argument("--dq-mode", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -18,6 +18,27 @@ REL_L2 = 1e-2
 MAX_ABS = 3e-2
 
 
+def structural_zero_rows(case: si.Case):
+    """Rows whose gradients are exactly zero by construction, independent of
+    rounding: padding rows, queries of sequences without keys, and keys that
+    no query sees (sequences without queries; keys j >= s1 under the
+    top-left causal mask)."""
+    zq = np.zeros(case.total_q, dtype=bool)
+    zk = np.zeros(case.total_kv, dtype=bool)
+    zq[int(case.cu_q[-1]):] = True
+    zk[int(case.cu_kv[-1]):] = True
+    for b in range(case.batch):
+        q0, q1 = int(case.cu_q[b]), int(case.cu_q[b + 1])
+        k0, k1 = int(case.cu_kv[b]), int(case.cu_kv[b + 1])
+        if k1 == k0:
+            zq[q0:q1] = True
+        if q1 == q0:
+            zk[k0:k1] = True
+        elif case.causal:
+            zk[k0 + min(q1 - q0, k1 - k0):k1] = True
+    return zq, zk
+
+
 def compare(name, got, ref, exact_zero_mask=None):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -31,9 +52,9 @@ def compare(name, got, ref, exact_zero_mask=None):
     mx = np.abs(got - ref).max()
     assert rel <= REL_L2, f"{name}: relative L2 error {rel:.3e} > {REL_L2}"
     assert mx <= MAX_ABS * np.abs(ref).max(), f"{name}: max abs error {mx:.3e} > {MAX_ABS} * {np.abs(ref).max():.3e}"
-    zmask = (ref == 0) if exact_zero_mask is None else exact_zero_mask
-    bad = np.count_nonzero(got[zmask] != 0)
-    assert bad == 0, f"{name}: {bad} non-zero values where the result must be exactly 0"
+    if exact_zero_mask is not None:
+        bad = np.count_nonzero(got[exact_zero_mask] != 0)
+        assert bad == 0, f"{name}: {bad} non-zero values where the result must be exactly 0"
     return rel
 
 
@@ -99,16 +120,19 @@ def check_case(prep: Prepared, out=None, dq_mode=0):
     units = prep.heads_subset or [(b, h) for b in range(case.batch) for h in range(case.heads)]
     got = (to_np(dq), to_np(dk), to_np(dv))
     errs = {}
+    zq, zk = structural_zero_rows(case)
     if prep.heads_subset is None:
-        for name, g, r in zip(("dq", "dk", "dv"), got, ref[:3]):
-            errs[name] = compare(name, g, r)
+        for name, g, r, z in zip(("dq", "dk", "dv"), got, ref[:3], (zq, zk, zk)):
+            errs[name] = compare(name, g, r, np.broadcast_to(z[:, None, None], g.shape))
     else:
         for b, h in units:
             qr = slice(int(case.cu_q[b]), int(case.cu_q[b + 1]))
             kr = slice(int(case.cu_kv[b]), int(case.cu_kv[b + 1]))
-            for name, g, r, rows in zip(("dq", "dk", "dv"), got, ref[:3], (qr, kr, kr)):
-                errs[f"{name}[{b},{h}]"] = compare(f"{name}[b={b},h={h}]", g[rows, h], r[rows, h])
-    # padding rows past the last sequence are exactly zero for every head
-    nq, nkv = int(case.cu_q[-1]), int(case.cu_kv[-1])
-    assert np.all(got[0][nq:] == 0) and np.all(got[1][nkv:] == 0) and np.all(got[2][nkv:] == 0)
+            for name, g, r, rows, z in zip(("dq", "dk", "dv"), got, ref[:3], (qr, kr, kr), (zq, zk, zk)):
+                gg = g[rows, h]
+                errs[f"{name}[{b},{h}]"] = compare(f"{name}[b={b},h={h}]", gg, r[rows, h],
+                                                   np.broadcast_to(z[rows][:, None], gg.shape))
+    # structural zeros hold for every head, checked or not
+    for g, z in ((got[0], zq), (got[1], zk), (got[2], zk)):
+        assert np.all(g[z] == 0), "non-zero gradient in a padding row or a row no query/key reaches"
     return errs
