@@ -81,18 +81,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A [rows, heads*head_dim] bf16 view with 64 x 128 boxes and 128-byte
-// swizzle; rows past `rows` read as zero.
-int make_map(CUtensorMap* m, const void* base, int rows, int heads, int head_dim, const char* name) {
+// A [rows, heads*head_dim] view with 128-byte swizzle: bf16 with 64 x 128
+// boxes (operand tiles; rows past `rows` read as zero), or fp32 with
+// 32 x 32 boxes (the dQ accumulator; rows past `rows` are not written).
+int make_map(CUtensorMap* m, const void* base, int rows, int heads, int head_dim, const char* name,
+             bool fp32 = false) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t esize = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * head_dim, static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * head_dim * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * head_dim * esize};
+  cuuint32_t box[2] = {fp32 ? 32u : 64u, fp32 ? 32u : 128u};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
   return FA_OK;
 }
@@ -237,6 +240,7 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
   if ((rc = make_map(&p.tm_k, k, total_kv, heads, head_dim, "k"))) return rc;
   if ((rc = make_map(&p.tm_v, v, total_kv, heads, head_dim, "v"))) return rc;
   if ((rc = make_map(&p.tm_do, dobase, max_q > 0 ? total_q : total_kv, heads, head_dim, "dout"))) return rc;
+  if (max_q > 0 && (rc = make_map(&p.tm_dq, dq_acc, total_q, heads, head_dim, "dq_acc", true))) return rc;
   p.m = m;
   p.l = l;
   p.D = D;

@@ -8,7 +8,8 @@
 // is the key-block-outer one that section 1 names as best for dK/dV: a CTA
 // owns one (sequence, head, 128-row key block), keeps dK and dV in tensor
 // memory across its whole query sweep and adds each dQ partial into an
-// fp32 accumulator (section 3, V2 atomic write-back, restricted to dQ).
+// fp32 accumulator in global memory (section 3, V2 atomic write-back,
+// restricted to dQ).
 //
 // Per query block i (128 rows), with the key block j fixed (128 rows):
 //   C1   S^T  = K_j Q_i^T              (TMEM cols [0,128), fp32)
@@ -19,20 +20,22 @@
 //        dS -> bf16 into shared memory (operand of dK and dQ)
 //   C2   dV_j += P^T dO_i              (TMEM cols [256, 256+d))
 //        dK_j += dS^T Q_i              (TMEM cols [256+d, 256+2d))
-//        dQ partial = dS K_j           (reuses TMEM cols [128,256))
-//   V2   dq_acc[rows of i] += partial  (fp32 atomics; scale applied later)
+//        dQ_i partial = dS K_j         (query rows on lanes; reuses the dP columns)
+//   V2   dq_acc[rows of i] += partial  (TMA tensor reduce-add from a swizzled
+//                                      shared-memory copy; scale applied later)
 // Transposed scores put key rows on TMEM lanes, so the softmax threads own
 // whole key rows and P / dS come out already in the layouts the C2 MMAs
-// want.  For d = 128 the dQ partial is produced transposed (d on lanes) so
-// that the atomic write-back of each warp covers 128 contiguous bytes.
+// want.  The MMA order inside one query block is dP_i, dV_i, S_{i+1},
+// dK_i, dQ_i: the next block's scores are computed while the softmax
+// warps derive dS_i.
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: K, V once; Q, dO and per-row stats per block
 //               (2-stage ring); zeroes rows past a sequence end
-//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
 //   warps 4-11  two softmax warpgroups, each owning 64 of the 128 query
 //               columns for all 128 key rows; at the end dV (4-7), dK (8-11)
-//   warps 12-15 dQ write-back
+//   warps 12-15 dQ write-back: TMEM -> shared memory -> TMA reduce-add
 // Every mbarrier wait is bounded (see sm103.cuh); on a timeout the CTA
 // records FA_ERR_TIMEOUT in the status word, drains and frees TMEM.
 #include <cuda.h>
@@ -60,7 +63,7 @@ constexpr uint32_t COL_DV = 256;
 // mbarrier slots
 enum {
   B_KV_FULL = 0, B_KV_READY, B_Q_FULL0, B_Q_FULL1, B_Q_READY0, B_Q_READY1, B_Q_EMPTY0, B_Q_EMPTY1,
-  B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_EMPTY, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
+  B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
   B_TEARDOWN, NUM_BARS
 };
 
@@ -72,7 +75,8 @@ struct Layout {
   static constexpr uint32_t V = TILE;
   static constexpr uint32_t Q = 2 * TILE;         // 2 stages
   static constexpr uint32_t DO = 4 * TILE;        // 2 stages
-  static constexpr uint32_t DS = 6 * TILE;        // [128 key rows, 128 query cols] bf16 = 32 KB
+  static constexpr uint32_t DS = 6 * TILE;        // [128 key rows, 128 query cols] bf16 = 32 KB;
+                                                  // doubles as the dQ staging area
   static constexpr uint32_t STATS = DS + 32768;   // per stage: lse2[128], D[128] (fp32)
   static constexpr uint32_t BARS = STATS + 2 * 2 * 128 * 4;
   static constexpr uint32_t MISC = BARS + NUM_BARS * 8;   // abort flag, TMEM address
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     mbar_init(bar(B_P_READY), 256);
     mbar_init(bar(B_P_USED), 1);
     mbar_init(bar(B_DS_READY), 256);
-    mbar_init(bar(B_DS_EMPTY), 1);
+    mbar_init(bar(B_DS_FREE), 4);
     mbar_init(bar(B_DQ_FULL), 1);
     mbar_init(bar(B_DQ_EMPTY), 128);
     mbar_init(bar(B_ACC_FULL), 1);
@@ -206,6 +210,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const int qb = qb0 + k;
         const int q_row0 = q_start + qb * BN;
         const int q_valid = min(BN, s1 - qb * BN);
+        // Row statistics first (they do not need the stage to be free):
+        // lse2 = m*log2(e) + log2(l), and D.
+        float lse2[4], dd[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;
+          lse2[j] = 0.f;
+          dd[j] = 0.f;
+          if (r < q_valid) {
+            const long long idx = static_cast<long long>(q_row0 + r) * H + h;
+            lse2[j] = p.m[idx] * 1.4426950408889634f + __log2f(p.l[idx]);
+            dd[j] = p.D[idx];
+          }
+        }
         if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), ((k >> 1) - 1) & 1, abort, status)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), 2 * L::TILE);
@@ -217,17 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         pend_bar = B_Q_FULL0 + s;
         pend_par = (k >> 1) & 1;
-        // Row statistics: lse2 = m*log2(e) + log2(l), and D.
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int r = lane + 32 * j;
-          float lse2 = 0.f, dd = 0.f;
-          if (r < q_valid) {
-            const long long idx = static_cast<long long>(q_row0 + r) * H + h;
-            lse2 = p.m[idx] * 1.4426950408889634f + __log2f(p.l[idx]);
-            dd = p.D[idx];
-          }
-          st_lse[s * 128 + r] = lse2;
-          st_D[s * 128 + r] = dd;
+          st_lse[s * 128 + lane + 32 * j] = lse2[j];
+          st_D[s * 128 + lane + 32 * j] = dd[j];
         }
         if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;
         pend_bar = -1;
@@ -246,66 +257,85 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (n_it > 0 && lane == 0) {
+    // The whole warp runs the schedule and waits; one elected lane issues.
+    if (n_it > 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);     // S^T, dP^T: K-major x K-major
       constexpr uint32_t ID_KV = idesc_bf16(128, D, 0, 1);      // dV, dK: B (dO / Q) MN-major
-      constexpr uint32_t ID_DQ = (D == 128) ? idesc_bf16(128, 128, 1, 1)   // dQ^T = K^T dS^T
-                                            : idesc_bf16(128, 64, 1, 1);   // dQ = dS K
+      constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);      // dQ = dS K: both MN-major
       const uint32_t t_s = tmem + COL_S, t_dp = tmem + COL_DP;
       const uint32_t t_dv = tmem + COL_DV, t_dk = tmem + L::COL_DK;
       const uint32_t sK = sbase + L::K, sV = sbase + L::V, sDS = sbase + L::DS;
-      bool ok = mbar_wait(bar(B_KV_READY), 0, abort, status);
+      bool ok = mbar_wait(bar(B_KV_READY), 0, abort, status) && mbar_wait(bar(B_Q_READY0), 0, abort, status);
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int t = 0; t < D / 16; ++t)
+            mma_ss(t_s, desc_kmajor(sK, t), desc_kmajor(sbase + L::Q, t), ID_S, t > 0);
+          mma_commit(bar(B_S_FULL));
+        }
+        __syncwarp();
+      }
       for (int k = 0; ok && k < n_it; ++k) {
         const int s = k & 1;
         const uint32_t ph = k & 1;
         const uint32_t sQ = sbase + L::Q + s * L::TILE, sDO = sbase + L::DO + s * L::TILE;
-        if (!mbar_wait(bar(B_Q_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
-        // P of the previous block (read by its dV MMAs) lives in the S columns.
-        if (k > 0 && !mbar_wait(bar(B_P_USED), (k - 1) & 1, abort, status)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < D / 16; ++t) mma_ss(t_s, desc_kmajor(sK, t), desc_kmajor(sQ, t), ID_S, t > 0);
-        mma_commit(bar(B_S_FULL));
-        // The previous dQ partial occupies the dP columns until written back.
+        // dP^T into the dP columns, free once the previous dQ partial is read out.
         if (k > 0 && !mbar_wait(bar(B_DQ_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int t = 0; t < D / 16; ++t) mma_ss(t_dp, desc_kmajor(sV, t), desc_kmajor(sDO, t), ID_S, t > 0);
-        mma_commit(bar(B_DP_FULL));
+          for (int t = 0; t < D / 16; ++t) mma_ss(t_dp, desc_kmajor(sV, t), desc_kmajor(sDO, t), ID_S, t > 0);
+          mma_commit(bar(B_DP_FULL));
+        }
+        __syncwarp();
         // dV += P^T dO with P (bf16) read from TMEM.
         if (!mbar_wait(bar(B_P_READY), ph, abort, status)) { ok = false; break; }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int t = 0; t < BN / 16; ++t)   // P of query rows 16t.. sits at column 64*(t/4) + 8*(t%4)
-          mma_ts(t_dv, t_s + (t >> 2) * 64 + (t & 3) * 8, desc_mnmajor(sDO, t), ID_KV, (k > 0 || t > 0));
-        mma_commit(bar(B_P_USED));
+          for (int t = 0; t < BN / 16; ++t)   // P of query rows 16t.. sits at column 64*(t/4) + 8*(t%4)
+            mma_ts(t_dv, t_s + (t >> 2) * 64 + (t & 3) * 8, desc_mnmajor(sDO, t), ID_KV, (k > 0 || t > 0));
+          mma_commit(bar(B_P_USED));
+        }
+        __syncwarp();
+        // Next block's S^T overwrites the S columns once dV has consumed P.
+        if (k + 1 < n_it) {
+          const int s1n = (k + 1) & 1;
+          if (!mbar_wait(bar(B_Q_READY0 + s1n), ((k + 1) >> 1) & 1, abort, status)) { ok = false; break; }
+          if (!mbar_wait(bar(B_P_USED), ph, abort, status)) { ok = false; break; }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t sQn = sbase + L::Q + s1n * L::TILE;
+#pragma unroll
+            for (int t = 0; t < D / 16; ++t) mma_ss(t_s, desc_kmajor(sK, t), desc_kmajor(sQn, t), ID_S, t > 0);
+            mma_commit(bar(B_S_FULL));
+          }
+          __syncwarp();
+        }
         // dK += dS^T Q and the dQ partial, both from dS in shared memory.
         if (!mbar_wait(bar(B_DS_READY), ph, abort, status)) { ok = false; break; }
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int t = 0; t < BN / 16; ++t)
-          mma_ss(t_dk, desc_kmajor(sDS, t), desc_mnmajor(sQ, t), ID_KV, (k > 0 || t > 0));
-        if (D == 128) {
-#pragma unroll
-          for (int t = 0; t < BM / 16; ++t) mma_ss(t_dp, desc_mnmajor(sK, t), desc_mnmajor(sDS, t), ID_DQ, t > 0);
-        } else {
+          for (int t = 0; t < BN / 16; ++t)
+            mma_ss(t_dk, desc_kmajor(sDS, t), desc_mnmajor(sQ, t), ID_KV, (k > 0 || t > 0));
 #pragma unroll
           for (int t = 0; t < BM / 16; ++t) mma_ss(t_dp, desc_mnmajor(sDS, t), desc_mnmajor(sK, t), ID_DQ, t > 0);
+          mma_commit(bar(B_DQ_FULL));
+          mma_commit(bar(B_Q_EMPTY0 + s));
         }
-        mma_commit(bar(B_DS_EMPTY));
-        mma_commit(bar(B_DQ_FULL));
-        mma_commit(bar(B_Q_EMPTY0 + s));
+        __syncwarp();
       }
-      if (ok) {
-        mma_commit(bar(B_ACC_FULL));
-      } else {
+      ok = __all_sync(0xffffffffu, ok);
+      if (elect_one()) mma_commit(bar(ok ? B_ACC_FULL : B_TEARDOWN));
+      __syncwarp();
+      if (!ok) {
         // Aborted: wait (bounded) for every MMA issued so far before TMEM is freed.
-        mma_commit(bar(B_TEARDOWN));
         volatile int no_abort = 0;
         mbar_wait(bar(B_TEARDOWN), 0, &no_abort, status);
       }
     }
-    __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / dS
     const int wg = (warp - 4) >> 2;          // 0: query columns 0-63, 1: 64-127
@@ -321,13 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const int q_valid = min(BN, s1 - qb * BN);
       const bool diag = p.causal && (qb == kvb);
       const bool need_mask = diag || q_valid < BN || kv_valid < BM;
-      // query index - key index threshold for the top-left causal mask: column c
-      // (global within block) is visible from row r iff c >= r when qb == kvb.
       if (!mbar_wait(bar(B_Q_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
       if (!mbar_wait(bar(B_S_FULL), ph, abort, status)) { ok = false; break; }
       tc_fence_after();
-      const float* lse = st_lse + s * 128 + wg * 64;
-      const float* dvec = st_D + s * 128 + wg * 64;
+      const float4* lse4 = reinterpret_cast<const float4*>(st_lse + s * 128 + wg * 64);
+      const float4* dvec4 = reinterpret_cast<const float4*>(st_D + s * 128 + wg * 64);
       float P[64];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -335,15 +363,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         tmem_ld32(tmem + lane_addr + COL_S + wg * 64 + half * 32, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = half * 32 + c;          // within this warpgroup's 64 columns
-          float pv = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -lse[col]));
-          if (need_mask) {
-            const int qc = wg * 64 + col;
-            const bool vis = (r < kv_valid) && (qc < q_valid) && (!diag || qc >= r);
-            pv = vis ? pv : 0.f;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 lv = lse4[half * 8 + c4];
+          const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 * 4 + e;
+            const int col = half * 32 + c;        // within this warpgroup's 64 columns
+            float pv = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -la[e]));
+            if (need_mask) {
+              const int qc = wg * 64 + col;
+              // top-left causal: query qc sees key r iff qc >= r inside the diagonal block
+              const bool vis = (r < kv_valid) && (qc < q_valid) && (!diag || qc >= r);
+              pv = vis ? pv : 0.f;
+            }
+            P[col] = pv;
           }
-          P[col] = pv;
         }
         uint32_t pk[16];
 #pragma unroll
@@ -357,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       mbar_arrive(bar(B_P_READY));
 
       if (!mbar_wait(bar(B_DP_FULL), ph, abort, status)) { ok = false; break; }
-      if (k > 0 && !mbar_wait(bar(B_DS_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
+      // The dS buffer doubles as the previous block's dQ staging area.
+      if (k > 0 && !mbar_wait(bar(B_DS_FREE), (k - 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t ds_row = sbase + L::DS + wg * CHUNK + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
@@ -367,16 +403,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c0 = half * 32 + 2 * j;
-          float d0 = P[c0] * (__uint_as_float(v[2 * j]) - dvec[c0]);
-          float d1 = P[c0 + 1] * (__uint_as_float(v[2 * j + 1]) - dvec[c0 + 1]);
-          if (need_mask) {
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dv4 = dvec4[half * 8 + c4];
+          const float da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+          float ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = half * 32 + c4 * 4 + e;
+            ds[e] = P[c] * (__uint_as_float(v[c4 * 4 + e]) - da[e]);
             // P is already 0 where masked, but dP may hold garbage there.
-            d0 = (P[c0] != 0.f) ? d0 : 0.f;
-            d1 = (P[c0 + 1] != 0.f) ? d1 : 0.f;
+            if (need_mask) ds[e] = (P[c] != 0.f) ? ds[e] : 0.f;
           }
-          pk[j] = pack_bf16x2(d0, d1);
+          pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+          pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -418,49 +457,52 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ write-back
+    // TMEM lanes are query rows.  Each warp stages its 32 rows, 32 columns
+    // at a time, as 128B-swizzled [32 x 32] fp32 boxes in the dS buffer and
+    // reduce-adds them into dq_acc with TMA; two boxes per warp in flight.
     const int quarter = warp & 3;
-    const int t = quarter * 32 + lane;       // TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t stage = sbase + L::DS + quarter * 8192;    // two 4 KB boxes per warp
+    constexpr int NC = D / 32;                                // 32-column chunks
+    bool issued = false;
     for (int k = 0; k < n_it; ++k) {
       const int qb = qb0 + k;
-      const int q_valid = min(BN, s1 - qb * BN);
-      const long long q_row0 = q_start + qb * BN;
+      const int q_row0 = q_start + qb * BN;
       if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
       tc_fence_after();
-      if (D == 128) {
-        // lanes = head-dim index t, columns = query rows
-        float* base = p.dq_acc + q_row0 * rs + h * D + t;
 #pragma unroll
-        for (int ch = 0; ch < BN / 32; ++ch) {
+      for (int rnd = 0; rnd < NC / 2; ++rnd) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = rnd * 2 + j;
           uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + COL_DP + ch * 32, v);
+          tmem_ld32(tmem + lane_addr + COL_DP + c * 32, v);
           tmem_ld_wait();
+          const uint32_t row = stage + j * 4096 + lane * 128;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int q = ch * 32 + c;
-            if (q < q_valid) atomicAdd(base + q * rs, __uint_as_float(v[c]));
-          }
+          for (int g = 0; g < 8; ++g)
+            st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
         }
-      } else {
-        // lanes = query rows, columns = head-dim index
-        float* base = p.dq_acc + (q_row0 + t) * rs + h * D;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + COL_DP + ch * 32, v);
-          tmem_ld_wait();
-          if (t < q_valid) {
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-              atomicAdd(reinterpret_cast<float4*>(base + ch * 32 + c4 * 4),
-                        make_float4(__uint_as_float(v[4 * c4]), __uint_as_float(v[4 * c4 + 1]),
-                                    __uint_as_float(v[4 * c4 + 2]), __uint_as_float(v[4 * c4 + 3])));
-          }
+        if (rnd == NC / 2 - 1) {
+          // every TMEM column of this partial has been read
+          tc_fence_before();
+          mbar_arrive(bar(B_DQ_EMPTY));
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_reduce_add_2d(&p.tm_dq, stage + j * 4096, h * D + (rnd * 2 + j) * 32, q_row0 + quarter * 32);
+          bulk_commit();
+          bulk_wait_read0();
+          issued = true;
+        }
+        __syncwarp();
       }
-      tc_fence_before();
-      mbar_arrive(bar(B_DQ_EMPTY));
+      if (lane == 0) mbar_arrive(bar(B_DS_FREE));
     }
+    if (lane == 0 && issued) bulk_wait_all0();
   }
 
   tc_fence_before();

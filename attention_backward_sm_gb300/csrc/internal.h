@@ -16,6 +16,7 @@ struct BwdParams {
   CUtensorMap tm_k;   // [total_kv rows, H*d cols]
   CUtensorMap tm_v;
   CUtensorMap tm_do;  // [total_q rows, H*d cols]
+  CUtensorMap tm_dq;  // dq_acc: [total_q rows, H*d cols] fp32, box 32 x 32, 128B swizzle (reduce-add target)
   const float* m;
   const float* l;
   const float* D;
