@@ -35,7 +35,8 @@
 //   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
 //   warps 4-11  two softmax warpgroups, each owning 64 of the 128 query
 //               columns for all 128 key rows; at the end dV (4-7), dK (8-11)
-//   warps 12-15 dQ write-back: TMEM -> shared memory -> TMA reduce-add
+//   warps 12-15 dQ write-back: TMEM -> shared memory (half in the dS
+//               buffer, half in the block's own dO buffer) -> TMA reduce-add
 // Every mbarrier wait is bounded (see sm103.cuh); on a timeout the CTA
 // records FA_ERR_TIMEOUT in the status word, drains and frees TMEM.
 #include <cuda.h>
@@ -62,7 +63,9 @@ constexpr uint32_t COL_DV = 256;
 
 // mbarrier slots
 enum {
-  B_KV_FULL = 0, B_KV_READY, B_Q_FULL0, B_Q_FULL1, B_Q_READY0, B_Q_READY1, B_Q_EMPTY0, B_Q_EMPTY1,
+  B_KV_FULL = 0, B_KV_READY,
+  B_Q_FULL0, B_Q_FULL1, B_Q_READY0, B_Q_READY1, B_Q_EMPTY0, B_Q_EMPTY1,
+  B_DO_FULL0, B_DO_FULL1, B_DO_READY0, B_DO_READY1, B_DO_EMPTY0, B_DO_EMPTY1,
   B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
   B_TEARDOWN, NUM_BARS
 };
@@ -75,8 +78,7 @@ struct Layout {
   static constexpr uint32_t V = TILE;
   static constexpr uint32_t Q = 2 * TILE;         // 2 stages
   static constexpr uint32_t DO = 4 * TILE;        // 2 stages
-  static constexpr uint32_t DS = 6 * TILE;        // [128 key rows, 128 query cols] bf16 = 32 KB;
-                                                  // doubles as the dQ staging area
+  static constexpr uint32_t DS = 6 * TILE;        // [128 key rows, 128 query cols] bf16 = 32 KB
   static constexpr uint32_t STATS = DS + 32768;   // per stage: lse2[128], D[128] (fp32)
   static constexpr uint32_t BARS = STATS + 2 * 2 * 128 * 4;
   static constexpr uint32_t MISC = BARS + NUM_BARS * 8;   // abort flag, TMEM address
@@ -153,13 +155,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       mbar_init(bar(B_Q_FULL0 + s), 1);
       mbar_init(bar(B_Q_READY0 + s), 1);
       mbar_init(bar(B_Q_EMPTY0 + s), 1);
+      mbar_init(bar(B_DO_FULL0 + s), 1);
+      mbar_init(bar(B_DO_READY0 + s), 1);
+      mbar_init(bar(B_DO_EMPTY0 + s), 4);   // one arrive per dQ write-back warp
     }
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_DP_FULL), 1);
     mbar_init(bar(B_P_READY), 256);
     mbar_init(bar(B_P_USED), 1);
     mbar_init(bar(B_DS_READY), 256);
-    mbar_init(bar(B_DS_FREE), 4);
+    mbar_init(bar(B_DS_FREE), 4);     // one arrive per dQ write-back warp
     mbar_init(bar(B_DQ_FULL), 1);
     mbar_init(bar(B_DQ_EMPTY), 128);
     mbar_init(bar(B_ACC_FULL), 1);
@@ -192,12 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       }
       __syncwarp();
       // Loads issued but not yet seen complete must land before the CTA
-      // exits, even on the abort path: remember the barrier and its parity.
-      int pend_bar = B_KV_FULL;
-      uint32_t pend_par = 0;
+      // exits, even on the abort path: remember their barriers and parities.
+      int pend_kv = 1, pend_q = -1, pend_do = -1;
+      uint32_t par_q = 0, par_do = 0;
       bool ok = mbar_wait(bar(B_KV_FULL), 0, abort, status);
       if (ok) {
-        pend_bar = -1;
+        pend_kv = 0;
         if (kv_valid < BM) {
           zero_rows<D>(sbase + L::K, kv_valid, lane);
           fence_proxy_async_smem();
@@ -205,55 +210,84 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_KV_READY));
       }
-      for (int k = 0; ok && k < n_it; ++k) {
-        const int s = k & 1;
+      // Raw row statistics (m, l, D) of a block are loaded one block ahead
+      // into registers and only combined (lse2 = m*log2(e) + log2(l)) when
+      // stored, so their latency hides behind the waits of the current block.
+      float rm[4], rl[4], rd[4], nm[4], nl[4], nd[4];
+      auto load_stats = [&](int k, float (&a)[4], float (&b)[4], float (&c)[4]) {
         const int qb = qb0 + k;
-        const int q_row0 = q_start + qb * BN;
         const int q_valid = min(BN, s1 - qb * BN);
-        // Row statistics first (they do not need the stage to be free):
-        // lse2 = m*log2(e) + log2(l), and D.
-        float lse2[4], dd[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = lane + 32 * j;
-          lse2[j] = 0.f;
-          dd[j] = 0.f;
-          if (r < q_valid) {
-            const long long idx = static_cast<long long>(q_row0 + r) * H + h;
-            lse2[j] = p.m[idx] * 1.4426950408889634f + __log2f(p.l[idx]);
-            dd[j] = p.D[idx];
+          a[j] = 0.f;
+          b[j] = 1.f;
+          c[j] = 0.f;
+          if (k < n_it && r < q_valid) {
+            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + h;
+            a[j] = __ldg(p.m + idx);
+            b[j] = __ldg(p.l + idx);
+            c[j] = __ldg(p.D + idx);
           }
         }
-        if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), ((k >> 1) - 1) & 1, abort, status)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), 2 * L::TILE);
-          for (int c = 0; c < L::NCH; ++c) {
-            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, h * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
-            tma_load_2d(sbase + L::DO + s * L::TILE + c * CHUNK, &p.tm_do, h * D + c * 64, q_row0,
-                        bar(B_Q_FULL0 + s));
-          }
-        }
-        pend_bar = B_Q_FULL0 + s;
-        pend_par = (k >> 1) & 1;
+      };
+      load_stats(0, nm, nl, nd);
+      for (int k = 0; ok && k < n_it; ++k) {
+        const int s = k & 1;
+        const uint32_t prev = ((k >> 1) - 1) & 1;   // parity of this stage's previous release
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          st_lse[s * 128 + lane + 32 * j] = lse2[j];
-          st_D[s * 128 + lane + 32 * j] = dd[j];
+          rm[j] = nm[j];
+          rl[j] = nl[j];
+          rd[j] = nd[j];
+        }
+        load_stats(k + 1, nm, nl, nd);
+        const int qb = qb0 + k;
+        const int q_row0 = q_start + qb * BN;
+        const int q_valid = min(BN, s1 - qb * BN);
+        if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), L::TILE);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, h * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
+        }
+        pend_q = s;
+        par_q = (k >> 1) & 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          st_lse[s * 128 + lane + 32 * j] = rm[j] * 1.4426950408889634f + __log2f(rl[j]);
+          st_D[s * 128 + lane + 32 * j] = rd[j];
         }
         if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;
-        pend_bar = -1;
+        pend_q = -1;
         if (q_valid < BN) {
           zero_rows<D>(sbase + L::Q + s * L::TILE, q_valid, lane);
-          zero_rows<D>(sbase + L::DO + s * L::TILE, q_valid, lane);
           fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
+        if (k >= 2 && !mbar_wait(bar(B_DO_EMPTY0 + s), prev, abort, status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_DO_FULL0 + s), L::TILE);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(sbase + L::DO + s * L::TILE + c * CHUNK, &p.tm_do, h * D + c * 64, q_row0,
+                        bar(B_DO_FULL0 + s));
+        }
+        pend_do = s;
+        par_do = (k >> 1) & 1;
+        if (!mbar_wait(bar(B_DO_FULL0 + s), (k >> 1) & 1, abort, status)) break;
+        pend_do = -1;
+        if (q_valid < BN) {
+          zero_rows<D>(sbase + L::DO + s * L::TILE, q_valid, lane);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DO_READY0 + s));
       }
-      if (pend_bar >= 0) {
-        volatile int no_abort = 0;
-        mbar_wait(bar(pend_bar), pend_par, &no_abort, status);
-      }
+      volatile int no_abort = 0;
+      if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
+      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
+      if (pend_do >= 0) mbar_wait(bar(B_DO_FULL0 + pend_do), par_do, &no_abort, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -282,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const uint32_t sQ = sbase + L::Q + s * L::TILE, sDO = sbase + L::DO + s * L::TILE;
         // dP^T into the dP columns, free once the previous dQ partial is read out.
         if (k > 0 && !mbar_wait(bar(B_DQ_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
+        if (!mbar_wait(bar(B_DO_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
 #pragma unroll
@@ -392,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       mbar_arrive(bar(B_P_READY));
 
       if (!mbar_wait(bar(B_DP_FULL), ph, abort, status)) { ok = false; break; }
-      // The dS buffer doubles as the previous block's dQ staging area.
+      // The dS buffer holds half of the previous block's dQ staging until
+      // its TMA reduce has read it (which is after dK / dQ consumed dS).
       if (k > 0 && !mbar_wait(bar(B_DS_FREE), (k - 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t ds_row = sbase + L::DS + wg * CHUNK + (r >> 3) * 1024 + (r & 7) * 128;
@@ -457,50 +493,76 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ write-back
-    // TMEM lanes are query rows.  Each warp stages its 32 rows, 32 columns
-    // at a time, as 128B-swizzled [32 x 32] fp32 boxes in the dS buffer and
-    // reduce-adds them into dq_acc with TMA; two boxes per warp in flight.
+    // TMEM lanes are query rows.  The partial of block k leaves as
+    // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
+    // First half of the columns: staged in the dS buffer (free once dK_k and
+    // dQ_k have run), released to the softmax warps as soon as TMA has read
+    // it.  Second half: staged in block k's dO buffer (dead after dV_k),
+    // released to the producer afterwards.  Both halves are in flight at
+    // once; the SM's write-out bandwidth, not the staging, sets the pace.
     const int quarter = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t stage = sbase + L::DS + quarter * 8192;    // two 4 KB boxes per warp
-    constexpr int NC = D / 32;                                // 32-column chunks
+    constexpr int NC = D / 32;              // 32-column chunks: 2 or 4
+    constexpr int BPH = NC / 2;             // boxes per warp per half: 1 or 2
+    auto stage_box = [&](uint32_t box, const uint32_t (&v)[32]) {
+      const uint32_t row = box + lane * 128;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    };
     bool issued = false;
+    const uint32_t slot_a = sbase + L::DS + quarter * 8192;            // up to two 4 KB boxes per warp
     for (int k = 0; k < n_it; ++k) {
+      const int s = k & 1;
       const int qb = qb0 + k;
-      const int q_row0 = q_start + qb * BN;
+      const int y = q_start + qb * BN + quarter * 32;
+      const uint32_t slot_b = sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
       if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
       tc_fence_after();
-#pragma unroll
-      for (int rnd = 0; rnd < NC / 2; ++rnd) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int c = rnd * 2 + j;
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + COL_DP + c * 32, v);
-          tmem_ld_wait();
-          const uint32_t row = stage + j * 4096 + lane * 128;
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-        }
-        if (rnd == NC / 2 - 1) {
-          // every TMEM column of this partial has been read
-          tc_fence_before();
-          mbar_arrive(bar(B_DQ_EMPTY));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_reduce_add_2d(&p.tm_dq, stage + j * 4096, h * D + (rnd * 2 + j) * 32, q_row0 + quarter * 32);
-          bulk_commit();
-          bulk_wait_read0();
-          issued = true;
-        }
-        __syncwarp();
+      uint32_t va[32], vb[32];
+      tmem_ld32(tmem + lane_addr + COL_DP + 0, va);
+      tmem_ld32(tmem + lane_addr + COL_DP + 32, vb);
+      tmem_ld_wait();
+      stage_box(slot_a, va);
+      if (BPH == 2) stage_box(slot_a + 4096, vb);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_2d(&p.tm_dq, slot_a, h * D + 0, y);
+        if (BPH == 2) tma_reduce_add_2d(&p.tm_dq, slot_a + 4096, h * D + 32, y);
+        bulk_commit();
+        issued = true;
       }
-      if (lane == 0) mbar_arrive(bar(B_DS_FREE));
+      if (BPH == 2) {
+        tmem_ld32(tmem + lane_addr + COL_DP + 64, va);
+        tmem_ld32(tmem + lane_addr + COL_DP + 96, vb);
+        tmem_ld_wait();
+      }
+      // every TMEM column of this partial has been read
+      tc_fence_before();
+      mbar_arrive(bar(B_DQ_EMPTY));
+      if (BPH == 2) {
+        stage_box(slot_b, va);
+        stage_box(slot_b + 4096, vb);
+      } else {
+        stage_box(slot_b, vb);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (BPH == 2) {
+          tma_reduce_add_2d(&p.tm_dq, slot_b, h * D + 64, y);
+          tma_reduce_add_2d(&p.tm_dq, slot_b + 4096, h * D + 96, y);
+        } else {
+          tma_reduce_add_2d(&p.tm_dq, slot_b, h * D + 32, y);
+        }
+        bulk_commit();
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
+        mbar_arrive(bar(B_DS_FREE));
+        bulk_wait_read0();                                               // second half read
+        mbar_arrive(bar(B_DO_EMPTY0 + s));
+      }
+      __syncwarp();
     }
     if (lane == 0 && issued) bulk_wait_all0();
   }
