@@ -119,6 +119,18 @@ def fa_bwd_dq_finalize(dq_acc, dq, scale: float, stream=None):
     _check(lib().fa_bwd_dq_finalize(_ptr(dq_acc), _ptr(dq), total_q, heads, dim, float(scale), _stream(stream)))
 
 
+def fa_bwd_noalloc(q, k, v, o, do, m, l, dq, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool,
+                   scale: float, stream=None):
+    """Whole backward into caller-provided dq, dk, dv with the library's own
+    fixed scratch array (no device allocation anywhere on the call)."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv = int(k.shape[0])
+    _check(lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(m), _ptr(l), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1, total_q,
+                                total_kv, heads, dim, int(bool(causal)), float(scale), _stream(stream)))
+
+
 def fa_check_device_status(stream=None):
     _check(lib().fa_check_device_status(_stream(stream)))
 

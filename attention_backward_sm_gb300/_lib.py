@@ -23,6 +23,8 @@ SIGNATURES = {
     "fa_bwd": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                     _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]),
     "fa_bwd_dq_finalize": (_i, [_p, _p, _i, _i, _i, _f, _p]),
+    "fa_bwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                            _i, _i, _i, _i, _i, _i, _f, _p]),
     "fa_check_device_status": (_i, [_p]),
     "fa_last_error": (ctypes.c_char_p, []),
 }

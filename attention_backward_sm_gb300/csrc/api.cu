@@ -114,6 +114,16 @@ int check_device() {
 
 }  // namespace
 
+namespace fa {
+int set_last_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+}  // namespace fa
+
 extern "C" {
 
 const char* fa_last_error(void) { return g_err; }

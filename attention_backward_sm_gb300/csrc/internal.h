@@ -57,4 +57,7 @@ struct FwdParams {
 };
 cudaError_t launch_fwd_stats(const FwdParams& p, int head_dim, int batch, int max_q_blocks64, cudaStream_t s);
 
+// Records a message for fa_last_error() on the calling thread and returns code.
+int set_last_error(int code, const char* fmt, ...);
+
 }  // namespace fa

@@ -116,6 +116,35 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
 int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads,
                        int head_dim, float scale, fa_stream_t stream);
 
+/* Bytes of the library's fixed scratch array used by fa_bwd_noalloc. */
+#define FA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* The full backward (fa_bwd_preprocess -> fa_bwd in FA_DQ_ATOMIC mode ->
+ * fa_bwd_dq_finalize) without any caller-provided scratch and without any
+ * device allocation.  The SK-16 article has no counterpart: this is an
+ * interface for callers that cannot call cudaMalloc, such as runtimes that
+ * own all device memory through their own planner and give a kernel
+ * library nothing but its inputs and outputs, serving loops in which an
+ * allocation would stall the device, and hosts with a fixed device-memory
+ * budget.  The caller passes inputs (q, k, v, o, dout, m, l,
+ * offsets) and outputs (dq, dk, dv) with the layouts above.  D and the fp32
+ * dQ accumulator live in one static device array of
+ * FA_NOALLOC_SCRATCH_BYTES that every GPU which loads the library keeps
+ * until process exit; a problem needing more (total_q * heads *
+ * (head_dim + 1) * 4 bytes, rounded up) is rejected with
+ * FA_ERR_INVALID_ARG before anything is launched.  The first call on a
+ * device looks the array's device address up (cudaGetSymbolAddress) and
+ * caches it: make that first call before any stream capture.  Every call
+ * shares the array: calls whose work overlaps on the GPU race, so order
+ * them on one stream.  Each call re-zeroes what must start at zero. */
+int fa_bwd_noalloc(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* o,
+                   const fa_bf16* dout, const float* m, const float* l,
+                   fa_bf16* dq, fa_bf16* dk, fa_bf16* dv,
+                   const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+                   const int32_t* cu_q_host, const int32_t* cu_kv_host,
+                   int batch, int total_q, int total_kv, int heads, int head_dim,
+                   int causal, float scale, fa_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device status word
  * that bounded waits set.  Returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_CUDA. */
 int fa_check_device_status(fa_stream_t stream);
