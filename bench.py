@@ -45,6 +45,16 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, pg=None, device=None):
+    """Element-wise max of a list of floats over all ranks (timing only; the
+    data path has no collective)."""
+    if pg is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -303,10 +313,7 @@ def run_gpu(args):
     fab.fa_check_device_status()
     elapsed_ms = start.elapsed_time(end)
     bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    if pg is not None:
-        t = torch.tensor([elapsed_ms, bwd_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms, bwd_ms = float(t[0]), float(t[1])
+    elapsed_ms, bwd_ms = max_over_ranks([elapsed_ms, bwd_ms], pg, dev)
     ms_per_step = elapsed_ms / args.steps
     value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
 
@@ -338,10 +345,7 @@ def run_gpu(args):
         e2.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = s2.elapsed_time(e2) / n_e2e
-        if pg is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t[0])
+        e2e_ms = max_over_ranks([e2e_ms], pg, dev)[0]
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
