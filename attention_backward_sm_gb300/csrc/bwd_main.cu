@@ -29,7 +29,9 @@
 // dK_i, dQ_i: the next block's scores are computed while the softmax
 // warps derive dS_i.
 //
-// Warp roles (512 threads):
+// Warp roles (512 threads; registers per thread set per warpgroup: 56 for
+// warps 0-3, 176 for the softmax warpgroups, 96 for the write-back; the
+// sum, 64512, fits the 65536 the block is launched with):
 //   warp 0      TMA producer: K, V once; Q, dO and per-row stats per block
 //               (2-stage ring); zeroes rows past a sequence end
 //   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<56>();
     if (n_it > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&p.tm_q);
@@ -291,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    setmaxnreg_dec<56>();
     // The whole warp runs the schedule and waits; one elected lane issues.
     if (n_it > 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);     // S^T, dP^T: K-major x K-major
@@ -373,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / dS
+    setmaxnreg_inc<176>();
     const int wg = (warp - 4) >> 2;          // 0: query columns 0-63, 1: 64-127
     const int quarter = warp & 3;            // TMEM lane quarter
     const int r = quarter * 32 + lane;       // key row within the block
@@ -387,10 +392,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const bool diag = p.causal && (qb == kvb);
       const bool need_mask = diag || q_valid < BN || kv_valid < BM;
       if (!mbar_wait(bar(B_Q_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
-      if (!mbar_wait(bar(B_S_FULL), ph, abort, status)) { ok = false; break; }
-      tc_fence_after();
+      // The 64 per-column statistics are read into registers before the
+      // scores are waited for: shared-memory loads queue behind the MMAs'
+      // operand reads, so their latency is hidden here rather than inside
+      // the exp loop.
       const float4* lse4 = reinterpret_cast<const float4*>(st_lse + s * 128 + wg * 64);
       const float4* dvec4 = reinterpret_cast<const float4*>(st_D + s * 128 + wg * 64);
+      float4 lsev[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) lsev[i] = lse4[i];
+      if (!mbar_wait(bar(B_S_FULL), ph, abort, status)) { ok = false; break; }
+      tc_fence_after();
       float P[64];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -399,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         tmem_ld_wait();
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 lv = lse4[half * 8 + c4];
+          const float4 lv = lsev[half * 8 + c4];
           const float la[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -426,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       tc_fence_before();
       mbar_arrive(bar(B_P_READY));
 
+      float4 dv4v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) dv4v[i] = dvec4[i];
       if (!mbar_wait(bar(B_DP_FULL), ph, abort, status)) { ok = false; break; }
       // The dS buffer holds half of the previous block's dQ staging until
       // its TMA reduce has read it (which is after dK / dQ consumed dS).
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         uint32_t pk[16];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 dv4 = dvec4[half * 8 + c4];
+          const float4 dv4 = dv4v[half * 8 + c4];
           const float da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
           float ds[4];
 #pragma unroll
@@ -493,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ write-back
+    setmaxnreg_dec<96>();
     // TMEM lanes are query rows.  The partial of block k leaves as
     // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
     // First half of the columns: staged in the dS buffer (free once dK_k and
@@ -565,6 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       __syncwarp();
     }
     if (lane == 0 && issued) bulk_wait_all0();
+  } else {
+    setmaxnreg_dec<56>();   // warps 2 and 3 only wait at the final barrier
   }
 
   tc_fence_before();
