@@ -195,8 +195,8 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   int max_q = 0;
   for (int b = 0; b < batch; ++b) max_q = cu_q_host[b + 1] - cu_q_host[b] > max_q ? cu_q_host[b + 1] - cu_q_host[b] : max_q;
   ok();
-  // one int32 ticket per (batch, head, 128-row query block), rounded to 256 B
-  const size_t n = static_cast<size_t>(batch) * heads * ((max_q + 127) / 128);
+  // one int32 counter per (batch, head, 128-row query block, 32-row quarter), rounded to 256 B
+  const size_t n = static_cast<size_t>(batch) * heads * ((max_q + 127) / 128) * 4;
   return ((n * 4 + 255) / 256) * 256;
 }
 
@@ -210,7 +210,6 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
   if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
   if (dq_mode != FA_DQ_ATOMIC && dq_mode != FA_DQ_DETERMINISTIC)
     return fail(FA_ERR_INVALID_ARG, "dq_mode must be 0 or 1, got %d", dq_mode);
-  if (dq_mode == FA_DQ_DETERMINISTIC) return fail(FA_ERR_UNSUPPORTED, "FA_DQ_DETERMINISTIC is not available yet");
   if (!isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
   int max_q = 0, max_kv = 0;
   if ((rc = check_offsets(cu_q_host, batch, total_q, "cu_q", &max_q))) return rc;

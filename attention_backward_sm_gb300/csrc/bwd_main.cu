@@ -29,8 +29,8 @@
 // dK_i, dQ_i: the next block's scores are computed while the softmax
 // warps derive dS_i.
 //
-// Warp roles (512 threads; registers per thread set per warpgroup: 56 for
-// warps 0-3, 176 for the softmax warpgroups, 96 for the write-back; the
+// Warp roles (512 threads; registers per thread set per warpgroup: 48 for
+// warps 0-3, 176 for the softmax warpgroups, 104 for the write-back; the
 // sum, 64512, fits the 65536 the block is launched with):
 //   warp 0      TMA producer: K, V once; Q, dO and per-row stats per block
 //               (2-stage ring); zeroes rows past a sequence end
@@ -119,6 +119,79 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first, int lane) {
   }
 }
 
+// P phase of one softmax thread: key row r, this warpgroup's 64 query
+// columns.  Reads S^T from TMEM (taddr = row's lane, first column), forms
+// P = 2^(S*scale*log2e - lse2) (= exp(S*scale - m) / l), zeroes masked
+// entries when MASK, and stores P as bf16 into the first 32 of the 64
+// columns just read.  MASK is a template parameter so that full blocks run
+// a loop without any per-element mask work.
+template <bool MASK>
+__device__ __forceinline__ void softmax_p(uint32_t taddr, const float4 (&lsev)[16], float sl2, float (&P)[64], int r,
+                                          int qc0, int kv_valid, int q_valid, bool diag) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v[32];
+    tmem_ld32(taddr + half * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+      const float4 lv = lsev[half * 8 + c4];
+      const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int col = half * 32 + c4 * 4 + e;
+        float pv = ex2_approx(fmaf(__uint_as_float(v[c4 * 4 + e]), sl2, -la[e]));
+        if (MASK) {
+          const int qc = qc0 + col;
+          // top-left causal: query qc sees key r iff qc >= r inside the diagonal block
+          const bool vis = (r < kv_valid) && (qc < q_valid) && (!diag || qc >= r);
+          pv = vis ? pv : 0.f;
+        }
+        P[col] = pv;
+      }
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(P[half * 32 + 2 * j], P[half * 32 + 2 * j + 1]);
+    tmem_st16(taddr + half * 16, pk);
+  }
+  tmem_st_wait();
+}
+
+// dS phase of one softmax thread: dS = P * (dP - D) from dP^T in TMEM,
+// rounded to bf16 and written as row r of the 128B-swizzled dS tile.
+template <bool MASK>
+__device__ __forceinline__ void softmax_ds(uint32_t taddr, const float4 (&dv4v)[16], const float (&P)[64],
+                                           uint32_t ds_row, int r) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v[32];
+    tmem_ld32(taddr + half * 32, v);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+      const float4 dv4 = dv4v[half * 8 + c4];
+      const float da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+      float ds[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = half * 32 + c4 * 4 + e;
+        ds[e] = P[c] * (__uint_as_float(v[c4 * 4 + e]) - da[e]);
+        // P is already 0 where masked, but dP may hold garbage there.
+        if (MASK) ds[e] = (P[c] != 0.f) ? ds[e] : 0.f;
+      }
+      pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+      pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int gg = half * 4 + g;            // 16-byte granule within the 128-byte row
+      st_shared_v4(ds_row + ((gg ^ (r & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
@@ -185,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    setmaxnreg_dec<56>();
+    setmaxnreg_dec<48>();
     if (n_it > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&p.tm_q);
@@ -294,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    setmaxnreg_dec<56>();
+    setmaxnreg_dec<48>();
     // The whole warp runs the schedule and waits; one elected lane issues.
     if (n_it > 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);     // S^T, dP^T: K-major x K-major
@@ -404,37 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       if (!mbar_wait(bar(B_S_FULL), ph, abort, status)) { ok = false; break; }
       tc_fence_after();
       float P[64];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_addr + COL_S + wg * 64 + half * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 lv = lsev[half * 8 + c4];
-          const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c4 * 4 + e;
-            const int col = half * 32 + c;        // within this warpgroup's 64 columns
-            float pv = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -la[e]));
-            if (need_mask) {
-              const int qc = wg * 64 + col;
-              // top-left causal: query qc sees key r iff qc >= r inside the diagonal block
-              const bool vis = (r < kv_valid) && (qc < q_valid) && (!diag || qc >= r);
-              pv = vis ? pv : 0.f;
-            }
-            P[col] = pv;
-          }
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(P[half * 32 + 2 * j], P[half * 32 + 2 * j + 1]);
-        // P goes into columns this warpgroup has already read (the other
-        // warpgroup may still be reading its own half of S).
-        tmem_st16(tmem + lane_addr + COL_S + wg * 64 + half * 16, pk);
-      }
-      tmem_st_wait();
+      const uint32_t t_srow = tmem + lane_addr + COL_S + wg * 64;
+      if (need_mask)
+        softmax_p<true>(t_srow, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
+      else
+        softmax_p<false>(t_srow, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
       tc_fence_before();
       mbar_arrive(bar(B_P_READY));
 
@@ -447,33 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       if (k > 0 && !mbar_wait(bar(B_DS_FREE), (k - 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t ds_row = sbase + L::DS + wg * CHUNK + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_addr + COL_DP + wg * 64 + half * 32, v);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 dv4 = dv4v[half * 8 + c4];
-          const float da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-          float ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = half * 32 + c4 * 4 + e;
-            ds[e] = P[c] * (__uint_as_float(v[c4 * 4 + e]) - da[e]);
-            // P is already 0 where masked, but dP may hold garbage there.
-            if (need_mask) ds[e] = (P[c] != 0.f) ? ds[e] : 0.f;
-          }
-          pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-          pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int gg = half * 4 + g;            // 16-byte granule within the 128-byte row
-          st_shared_v4(ds_row + ((gg ^ (r & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-        }
-      }
+      const uint32_t t_dprow = tmem + lane_addr + COL_DP + wg * 64;
+      if (need_mask)
+        softmax_ds<true>(t_dprow, dv4v, P, ds_row, r);
+      else
+        softmax_ds<false>(t_dprow, dv4v, P, ds_row, r);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(B_DS_READY));
@@ -508,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ write-back
-    setmaxnreg_dec<96>();
+    setmaxnreg_dec<104>();
     // TMEM lanes are query rows.  The partial of block k leaves as
     // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
     // First half of the columns: staged in the dS buffer (free once dK_k and
@@ -526,6 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       for (int g = 0; g < 8; ++g)
         st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
     };
+    // Deterministic mode: the (query block, quarter) partials of a head are
+    // added in ascending key-block order.  Key block j waits until the
+    // counter of its rows reads j, sends both halves, waits for them to
+    // complete and then advances the counter.  Every earlier key block of
+    // the head was launched before this one and never waits on a later one.
+    const bool det = p.dq_mode != 0;
     bool issued = false;
     const uint32_t slot_a = sbase + L::DS + quarter * 8192;            // up to two 4 KB boxes per warp
     for (int k = 0; k < n_it; ++k) {
@@ -533,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const int qb = qb0 + k;
       const int y = q_start + qb * BN + quarter * 32;
       const uint32_t slot_b = sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
+      int* ticket = det ? p.tickets + (static_cast<long long>(b * H + h) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
       if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
       tc_fence_after();
       uint32_t va[32], vb[32];
@@ -543,7 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       if (BPH == 2) stage_box(slot_a + 4096, vb);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      bool turn = true;
+      if (lane == 0 && det) {
+        turn = wait_counter(ticket, kvb, abort, status);
+        fence_proxy_async_global();
+      }
+      if (lane == 0 && turn) {
         tma_reduce_add_2d(&p.tm_dq, slot_a, h * D + 0, y);
         if (BPH == 2) tma_reduce_add_2d(&p.tm_dq, slot_a + 4096, h * D + 32, y);
         bulk_commit();
@@ -565,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && turn) {
         if (BPH == 2) {
           tma_reduce_add_2d(&p.tm_dq, slot_b, h * D + 64, y);
           tma_reduce_add_2d(&p.tm_dq, slot_b + 4096, h * D + 96, y);
@@ -577,12 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         mbar_arrive(bar(B_DS_FREE));
         bulk_wait_read0();                                               // second half read
         mbar_arrive(bar(B_DO_EMPTY0 + s));
+        if (det) {
+          bulk_wait_all0();                 // this block's additions are complete
+          fence_proxy_async_global();
+          __threadfence();
+          atomicAdd(ticket, 1);
+        }
       }
+      if (__any_sync(0xffffffffu, lane == 0 && !turn)) break;
       __syncwarp();
     }
     if (lane == 0 && issued) bulk_wait_all0();
   } else {
-    setmaxnreg_dec<56>();   // warps 2 and 3 only wait at the final barrier
+    setmaxnreg_dec<48>();   // warps 2 and 3 only wait at the final barrier
   }
 
   tc_fence_before();

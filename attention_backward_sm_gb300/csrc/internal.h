@@ -25,7 +25,7 @@ struct BwdParams {
   uint16_t* dv;
   const int32_t* cu_q;
   const int32_t* cu_kv;
-  int* tickets;        // deterministic mode: one counter per (batch, head, query block)
+  int* tickets;        // deterministic mode: one counter per (batch, head, query block, 32-row quarter)
   int heads;
   int causal;
   int dq_mode;

@@ -84,6 +84,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Waits until the global counter *t reaches `want` (acquire, gpu scope),
+// with the same time limit as mbar_wait.
+__device__ __forceinline__ bool wait_counter(const int* t, int want, volatile int* abort, int* status) {
+  const unsigned long long t0 = globaltimer();
+#pragma unroll 1
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(t) : "memory");
+    if (v >= want) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicCAS(status, 0, kStatusTimeout);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Orders the generic-proxy view of global memory with the async proxy
+// (TMA) in both directions.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(desc)) : "memory");

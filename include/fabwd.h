@@ -59,7 +59,9 @@ enum fa_status {
 
 enum fa_dq_mode {
     FA_DQ_ATOMIC = 0,         /* dQ partials added with fp32 atomics, in any order */
-    FA_DQ_DETERMINISTIC = 1   /* dQ partials added in ascending key-block order: bitwise reproducible */
+    FA_DQ_DETERMINISTIC = 1   /* dQ partials added in ascending key-block order: bitwise reproducible;
+                                 needs fa_bwd_workspace_size() bytes of workspace (one int32 counter
+                                 per batch x head x 128-row query block x 32-row quarter) */
 };
 
 /* Forward statistics used to build consistent backward inputs (support

@@ -118,3 +118,33 @@ def test_single_key_degenerate(d):
     bound_k = 2.0 ** -14 * case.softmax_scale * (noise[:, :, None] * np.abs(q)).sum(axis=0)
     assert np.all(np.abs(to_np(dq)) <= bound_q + 1e-30)
     assert np.all(np.abs(to_np(dk)[0]) <= bound_k + 1e-30)
+
+
+@pytest.mark.parametrize("case", [
+    si.fixed("det_d128_causal_tail", 2, 3, 128, 700, 700, True, 51),
+    si.Case("det_d64_varlen_cross", 3, 64, [300, 1, 513], [257, 700, 129], False, 52, pad_q=5, pad_kv=3),
+], ids=lambda c: c.name)
+def test_deterministic_mode(case):
+    """FA_DQ_DETERMINISTIC: parity with the oracle, and dQ bitwise identical
+    across runs (partials are added in ascending key-block order)."""
+    import attention_backward_sm_gb300 as fab
+    prep = Prepared(case)
+    first = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
+    check_case(prep, out=first)
+    for _ in range(2):
+        again = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+
+
+def test_deterministic_full_size_cfg3_causal_bitwise():
+    """Full-size causal batch in deterministic mode: two runs agree bit for bit
+    and the sampled heads match the oracle."""
+    import attention_backward_sm_gb300 as fab
+    case = si.cfg3(True)
+    subset = sampled(case, 2, seed=7)
+    prep = Prepared(case, heads_subset=subset)
+    first = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
+    check_case(prep, out=first)
+    again = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
+    assert torch.equal(first[0], again[0])
