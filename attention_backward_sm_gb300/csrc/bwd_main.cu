@@ -30,8 +30,9 @@
 // warps derive dS_i.
 //
 // Warp roles (512 threads; registers per thread set per warpgroup: 48 for
-// warps 0-3, 176 for the softmax warpgroups, 104 for the write-back; the
-// sum, 64512, fits the 65536 the block is launched with):
+// warps 0-3, 152 for the softmax warpgroups, 152 for the write-back, which
+// holds a whole 128-column dQ partial; the sum, 64512, fits the 65536 the
+// block is launched with):
 //   warp 0      TMA producer: K, V once; Q, dO and per-row stats per block
 //               (2-stage ring); zeroes rows past a sequence end
 //   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
@@ -55,6 +56,13 @@ __device__ int g_bwd_status = 0;
 namespace {
 
 constexpr int kThreads = 512;
+// Registers per thread: the block launches with 65536 / 512 = 128 and each
+// warpgroup then moves to its own budget.
+constexpr uint32_t kRegLaunch = 65536 / kThreads;
+constexpr uint32_t kRegOther = 48;     // warps 0-3: producer, MMA issuer, two idle warps
+constexpr uint32_t kRegSoftmax = 152;  // warps 4-11
+constexpr uint32_t kRegDrain = 152;    // warps 12-15
+static_assert(128 * kRegOther + 256 * kRegSoftmax + 128 * kRegDrain <= 65536, "register budgets exceed the launch");
 constexpr int BM = 128;   // key rows per CTA
 constexpr int BN = 128;   // query rows per block
 constexpr uint32_t CHUNK = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
@@ -97,6 +105,29 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int t) {
   return sw128_desc(tile + t * 2048, CHUNK, 1024);
 }
 
+// MMA groups over n 16-element K steps, issued by one thread.  The loops are
+// kept rolled: the issuing warp runs on a small register budget.
+// acc: whether the first step accumulates into D.
+__device__ __forceinline__ void mmas_kk(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
+#pragma unroll 1
+  for (int t = 0; t < n; ++t) mma_ss(d, desc_kmajor(a_tile, t), desc_kmajor(b_tile, t), idesc, acc | (t > 0));
+}
+__device__ __forceinline__ void mmas_km(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
+#pragma unroll 1
+  for (int t = 0; t < n; ++t) mma_ss(d, desc_kmajor(a_tile, t), desc_mnmajor(b_tile, t), idesc, acc | (t > 0));
+}
+__device__ __forceinline__ void mmas_mm(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
+#pragma unroll 1
+  for (int t = 0; t < n; ++t) mma_ss(d, desc_mnmajor(a_tile, t), desc_mnmajor(b_tile, t), idesc, acc | (t > 0));
+}
+// A from TMEM: P of K step t sits at column 64*(t/4) + 8*(t%4) (each softmax
+// warpgroup keeps its 64 query columns' P in the first 32 of its 64 columns).
+__device__ __forceinline__ void mmas_tm(uint32_t d, uint32_t a_tmem, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
+#pragma unroll 1
+  for (int t = 0; t < n; ++t)
+    mma_ts(d, a_tmem + (t >> 2) * 64 + (t & 3) * 8, desc_mnmajor(b_tile, t), idesc, acc | (t > 0));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -125,17 +156,25 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first, int lane) {
 // entries when MASK, and stores P as bf16 into the first 32 of the 64
 // columns just read.  MASK is a template parameter so that full blocks run
 // a loop without any per-element mask work.
+// lse4: the 64 per-column lse2 values in shared memory; pre: the first 32
+// of them, read earlier.  The second 32 are read while the first TMEM load
+// is in flight.
 template <bool MASK>
-__device__ __forceinline__ void softmax_p(uint32_t taddr, const float4 (&lsev)[16], float sl2, float (&P)[64], int r,
-                                          int qc0, int kv_valid, int q_valid, bool diag) {
+__device__ __forceinline__ void softmax_p(uint32_t taddr, const float4* lse4, const float4 (&pre)[8], float sl2,
+                                          float (&P)[64], int r, int qc0, int kv_valid, int q_valid, bool diag) {
+  float4 nxt[8];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint32_t v[32];
     tmem_ld32(taddr + half * 32, v);
+    if (half == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nxt[i] = lse4[8 + i];
+    }
     tmem_ld_wait();
 #pragma unroll
     for (int c4 = 0; c4 < 8; ++c4) {
-      const float4 lv = lsev[half * 8 + c4];
+      const float4 lv = half == 0 ? pre[c4] : nxt[c4];
       const float la[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -160,18 +199,24 @@ __device__ __forceinline__ void softmax_p(uint32_t taddr, const float4 (&lsev)[1
 
 // dS phase of one softmax thread: dS = P * (dP - D) from dP^T in TMEM,
 // rounded to bf16 and written as row r of the 128B-swizzled dS tile.
+// dvec4: the 64 per-column D values in shared memory; pre: the first 32.
 template <bool MASK>
-__device__ __forceinline__ void softmax_ds(uint32_t taddr, const float4 (&dv4v)[16], const float (&P)[64],
-                                           uint32_t ds_row, int r) {
+__device__ __forceinline__ void softmax_ds(uint32_t taddr, const float4* dvec4, const float4 (&pre)[8],
+                                           const float (&P)[64], uint32_t ds_row, int r) {
+  float4 nxt[8];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint32_t v[32];
     tmem_ld32(taddr + half * 32, v);
+    if (half == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nxt[i] = dvec4[8 + i];
+    }
     tmem_ld_wait();
     uint32_t pk[16];
 #pragma unroll
     for (int c4 = 0; c4 < 8; ++c4) {
-      const float4 dv4 = dv4v[half * 8 + c4];
+      const float4 dv4 = half == 0 ? pre[c4] : nxt[c4];
       const float da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
       float ds[4];
 #pragma unroll
@@ -258,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    setmaxnreg_dec<48>();
+    setmaxnreg_to<kRegOther, kRegLaunch>();
     if (n_it > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&p.tm_q);
@@ -367,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    setmaxnreg_dec<48>();
+    setmaxnreg_to<kRegOther, kRegLaunch>();
     // The whole warp runs the schedule and waits; one elected lane issues.
     if (n_it > 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);     // S^T, dP^T: K-major x K-major
@@ -380,9 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       if (ok) {
         tc_fence_after();
         if (elect_one()) {
-#pragma unroll
-          for (int t = 0; t < D / 16; ++t)
-            mma_ss(t_s, desc_kmajor(sK, t), desc_kmajor(sbase + L::Q, t), ID_S, t > 0);
+          mmas_kk(t_s, sK, sbase + L::Q, ID_S, D / 16, 0);
           mma_commit(bar(B_S_FULL));
         }
         __syncwarp();
@@ -396,8 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (!mbar_wait(bar(B_DO_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-#pragma unroll
-          for (int t = 0; t < D / 16; ++t) mma_ss(t_dp, desc_kmajor(sV, t), desc_kmajor(sDO, t), ID_S, t > 0);
+          mmas_kk(t_dp, sV, sDO, ID_S, D / 16, 0);
           mma_commit(bar(B_DP_FULL));
         }
         __syncwarp();
@@ -405,39 +447,59 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (!mbar_wait(bar(B_P_READY), ph, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-#pragma unroll
-          for (int t = 0; t < BN / 16; ++t)   // P of query rows 16t.. sits at column 64*(t/4) + 8*(t%4)
-            mma_ts(t_dv, t_s + (t >> 2) * 64 + (t & 3) * 8, desc_mnmajor(sDO, t), ID_KV, (k > 0 || t > 0));
+          mmas_tm(t_dv, t_s, sDO, ID_KV, BN / 16, k > 0);
           mma_commit(bar(B_P_USED));
         }
         __syncwarp();
-        // Next block's S^T overwrites the S columns once dV has consumed P.
-        if (k + 1 < n_it) {
+        // Two independent groups follow dV_i: the next block's S^T (needs
+        // Q_{i+1} loaded and dV_i done, since it overwrites the P columns)
+        // and this block's dK / dQ (need dS_i).  Issue whichever group's
+        // inputs are ready first; dK / dQ first when both are, because the
+        // dQ partial gates the next dP through the write-back.
+        {
+          bool need_s = (k + 1 < n_it), need_c2 = true;
           const int s1n = (k + 1) & 1;
-          if (!mbar_wait(bar(B_Q_READY0 + s1n), ((k + 1) >> 1) & 1, abort, status)) { ok = false; break; }
-          if (!mbar_wait(bar(B_P_USED), ph, abort, status)) { ok = false; break; }
-          tc_fence_after();
-          if (elect_one()) {
-            const uint32_t sQn = sbase + L::Q + s1n * L::TILE;
-#pragma unroll
-            for (int t = 0; t < D / 16; ++t) mma_ss(t_s, desc_kmajor(sK, t), desc_kmajor(sQn, t), ID_S, t > 0);
-            mma_commit(bar(B_S_FULL));
+          const uint32_t qpar = ((k + 1) >> 1) & 1;
+          const unsigned long long t0 = globaltimer();
+          while (need_s || need_c2) {
+            bool s_ready = need_s && mbar_test(bar(B_Q_READY0 + s1n), qpar) && mbar_test(bar(B_P_USED), ph);
+            bool c_ready = need_c2 && mbar_test(bar(B_DS_READY), ph);
+            s_ready = __shfl_sync(0xffffffffu, s_ready, 0);
+            c_ready = __shfl_sync(0xffffffffu, c_ready, 0);
+            if (s_ready && !c_ready) {
+              tc_fence_after();
+              if (elect_one()) {
+                mmas_kk(t_s, sK, sbase + L::Q + s1n * L::TILE, ID_S, D / 16, 0);
+                mma_commit(bar(B_S_FULL));
+              }
+              __syncwarp();
+              need_s = false;
+            } else if (c_ready) {
+              // dK += dS^T Q and the dQ partial, both from dS in shared memory.
+              tc_fence_after();
+              if (elect_one()) {
+                mmas_km(t_dk, sDS, sQ, ID_KV, BN / 16, k > 0);
+                mmas_mm(t_dp, sDS, sK, ID_DQ, BM / 16, 0);
+                mma_commit(bar(B_DQ_FULL));
+                mma_commit(bar(B_Q_EMPTY0 + s));
+              }
+              __syncwarp();
+              need_c2 = false;
+            } else {
+              const bool give_up = *abort || (globaltimer() - t0 > kWaitLimitNs);
+              if (__shfl_sync(0xffffffffu, give_up, 0)) {
+                if (lane == 0 && !*abort) {
+                  atomicCAS(status, 0, kStatusTimeout);
+                  *abort = 1;
+                }
+                ok = false;
+                break;
+              }
+              __nanosleep(32);
+            }
           }
-          __syncwarp();
+          if (!ok) break;
         }
-        // dK += dS^T Q and the dQ partial, both from dS in shared memory.
-        if (!mbar_wait(bar(B_DS_READY), ph, abort, status)) { ok = false; break; }
-        tc_fence_after();
-        if (elect_one()) {
-#pragma unroll
-          for (int t = 0; t < BN / 16; ++t)
-            mma_ss(t_dk, desc_kmajor(sDS, t), desc_mnmajor(sQ, t), ID_KV, (k > 0 || t > 0));
-#pragma unroll
-          for (int t = 0; t < BM / 16; ++t) mma_ss(t_dp, desc_mnmajor(sDS, t), desc_mnmajor(sK, t), ID_DQ, t > 0);
-          mma_commit(bar(B_DQ_FULL));
-          mma_commit(bar(B_Q_EMPTY0 + s));
-        }
-        __syncwarp();
       }
       ok = __all_sync(0xffffffffu, ok);
       if (elect_one()) mma_commit(bar(ok ? B_ACC_FULL : B_TEARDOWN));
@@ -450,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / dS
-    setmaxnreg_inc<176>();
+    setmaxnreg_to<kRegSoftmax, kRegLaunch>();
     const int wg = (warp - 4) >> 2;          // 0: query columns 0-63, 1: 64-127
     const int quarter = warp & 3;            // TMEM lane quarter
     const int r = quarter * 32 + lane;       // key row within the block
@@ -471,23 +533,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       // the exp loop.
       const float4* lse4 = reinterpret_cast<const float4*>(st_lse + s * 128 + wg * 64);
       const float4* dvec4 = reinterpret_cast<const float4*>(st_D + s * 128 + wg * 64);
-      float4 lsev[16];
+      float4 lsev[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) lsev[i] = lse4[i];
+      for (int i = 0; i < 8; ++i) lsev[i] = lse4[i];
       if (!mbar_wait(bar(B_S_FULL), ph, abort, status)) { ok = false; break; }
       tc_fence_after();
       float P[64];
       const uint32_t t_srow = tmem + lane_addr + COL_S + wg * 64;
       if (need_mask)
-        softmax_p<true>(t_srow, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
+        softmax_p<true>(t_srow, lse4, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
       else
-        softmax_p<false>(t_srow, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
+        softmax_p<false>(t_srow, lse4, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
       tc_fence_before();
       mbar_arrive(bar(B_P_READY));
 
-      float4 dv4v[16];
+      float4 dv4v[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) dv4v[i] = dvec4[i];
+      for (int i = 0; i < 8; ++i) dv4v[i] = dvec4[i];
       if (!mbar_wait(bar(B_DP_FULL), ph, abort, status)) { ok = false; break; }
       // The dS buffer holds half of the previous block's dQ staging until
       // its TMA reduce has read it (which is after dK / dQ consumed dS).
@@ -496,9 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const uint32_t ds_row = sbase + L::DS + wg * CHUNK + (r >> 3) * 1024 + (r & 7) * 128;
       const uint32_t t_dprow = tmem + lane_addr + COL_DP + wg * 64;
       if (need_mask)
-        softmax_ds<true>(t_dprow, dv4v, P, ds_row, r);
+        softmax_ds<true>(t_dprow, dvec4, dv4v, P, ds_row, r);
       else
-        softmax_ds<false>(t_dprow, dv4v, P, ds_row, r);
+        softmax_ds<false>(t_dprow, dvec4, dv4v, P, ds_row, r);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(B_DS_READY));
@@ -533,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ write-back
-    setmaxnreg_dec<104>();
+    setmaxnreg_to<kRegDrain, kRegLaunch>();
     // TMEM lanes are query rows.  The partial of block k leaves as
     // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
     // First half of the columns: staged in the dS buffer (free once dK_k and
@@ -567,10 +629,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       int* ticket = det ? p.tickets + (static_cast<long long>(b * H + h) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
       if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
       tc_fence_after();
-      uint32_t va[32], vb[32];
+      uint32_t va[32], vb[32], vc[32], vd[32];
       tmem_ld32(tmem + lane_addr + COL_DP + 0, va);
       tmem_ld32(tmem + lane_addr + COL_DP + 32, vb);
+      if (BPH == 2) {
+        tmem_ld32(tmem + lane_addr + COL_DP + 64, vc);
+        tmem_ld32(tmem + lane_addr + COL_DP + 96, vd);
+      }
       tmem_ld_wait();
+      // every TMEM column of this partial has been read
+      tc_fence_before();
+      mbar_arrive(bar(B_DQ_EMPTY));
       stage_box(slot_a, va);
       if (BPH == 2) stage_box(slot_a + 4096, vb);
       fence_proxy_async_smem();
@@ -587,16 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         issued = true;
       }
       if (BPH == 2) {
-        tmem_ld32(tmem + lane_addr + COL_DP + 64, va);
-        tmem_ld32(tmem + lane_addr + COL_DP + 96, vb);
-        tmem_ld_wait();
-      }
-      // every TMEM column of this partial has been read
-      tc_fence_before();
-      mbar_arrive(bar(B_DQ_EMPTY));
-      if (BPH == 2) {
-        stage_box(slot_b, va);
-        stage_box(slot_b + 4096, vb);
+        stage_box(slot_b, vc);
+        stage_box(slot_b + 4096, vd);
       } else {
         stage_box(slot_b, vb);
       }
@@ -626,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
     if (lane == 0 && issued) bulk_wait_all0();
   } else {
-    setmaxnreg_dec<48>();   // warps 2 and 3 only wait at the final barrier
+    setmaxnreg_to<kRegOther, kRegLaunch>();   // warps 2 and 3 only wait at the final barrier
   }
 
   tc_fence_before();

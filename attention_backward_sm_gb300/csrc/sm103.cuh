@@ -65,6 +65,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase completion.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up (and
 // records a timeout in *status and in *abort) after kWaitLimitNs, or as
 // soon as another thread of the CTA has set *abort.  Returns true on
@@ -147,6 +160,15 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Moves a warpgroup from the launch budget LAUNCH to N registers per
+// thread, choosing .inc or .dec at compile time (a .dec to a larger count,
+// or an .inc to a smaller one, is an illegal instruction).
+template <uint32_t N, uint32_t LAUNCH>
+__device__ __forceinline__ void setmaxnreg_to() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  if constexpr (N > LAUNCH) setmaxnreg_inc<N>();
+  else if constexpr (N < LAUNCH) setmaxnreg_dec<N>();
 }
 
 // One lane of a converged warp returns true.
