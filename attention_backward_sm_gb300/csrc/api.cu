@@ -37,6 +37,7 @@ int cuda_fail(cudaError_t e, const char* where) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+
 // Checks host offsets: batch+1 entries, cu[0] = 0, non-decreasing,
 // cu[batch] <= total.  Reports the longest sequence.
 int check_offsets(const int32_t* cu, int batch, int total, const char* name, int* max_len) {
@@ -262,6 +263,7 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
   p.causal = causal;
   p.dq_mode = dq_mode;
   p.max_q_blocks = (max_q + 127) / 128;
+  p.kv_reverse = (dq_mode == FA_DQ_DETERMINISTIC && causal) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tickets = static_cast<int*>(workspace);

@@ -245,7 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kvb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // Deterministic causal runs add dQ partials in descending key-block order
+  // and launch key blocks high to low, so that every CTA a CTA waits for was
+  // launched before it (see the dQ write-back).
+  const int kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                               : static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y, b = blockIdx.z;
   const int H = p.heads;
   const int q_start = p.cu_q[b], s1 = p.cu_q[b + 1] - q_start;
   const int kv_start = p.cu_kv[b], s2 = p.cu_kv[b + 1] - kv_start;
@@ -258,6 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   const int n_qb = (s1 + BN - 1) / BN;
   const int qb0 = p.causal ? kvb : 0;               // top-left mask: query block >= key block
   const int n_it = max(0, n_qb - qb0);
+  const int n_kvb = (s2 + BM - 1) / BM;
+  auto qb_of = [&](int k) { return qb0 + k; };
   const long long rs = static_cast<long long>(H) * D;   // row stride (elements)
 
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC);
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       // stored, so their latency hides behind the waits of the current block.
       float rm[4], rl[4], rd[4], nm[4], nl[4], nd[4];
       auto load_stats = [&](int k, float (&a)[4], float (&b)[4], float (&c)[4]) {
-        const int qb = qb0 + k;
+        const int qb = qb_of(k);
         const int q_valid = min(BN, s1 - qb * BN);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           rd[j] = nd[j];
         }
         load_stats(k + 1, nm, nl, nd);
-        const int qb = qb0 + k;
+        const int qb = qb_of(k);
         const int q_row0 = q_start + qb * BN;
         const int q_valid = min(BN, s1 - qb * BN);
         if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
@@ -522,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     for (int k = 0; k < n_it; ++k) {
       const int s = k & 1;
       const uint32_t ph = k & 1;
-      const int qb = qb0 + k;
+      const int qb = qb_of(k);
       const int q_valid = min(BN, s1 - qb * BN);
       const bool diag = p.causal && (qb == kvb);
       const bool need_mask = diag || q_valid < BN || kv_valid < BM;
@@ -623,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const uint32_t slot_a = sbase + L::DS + quarter * 8192;            // up to two 4 KB boxes per warp
     for (int k = 0; k < n_it; ++k) {
       const int s = k & 1;
-      const int qb = qb0 + k;
+      const int qb = qb_of(k);
       const int y = q_start + qb * BN + quarter * 32;
       const uint32_t slot_b = sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
       int* ticket = det ? p.tickets + (static_cast<long long>(b * H + h) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
@@ -646,7 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       __syncwarp();
       bool turn = true;
       if (lane == 0 && det) {
-        turn = wait_counter(ticket, kvb, abort, status);
+        // partials that come before this one: key blocks 0..kvb-1 (ascending
+        // order), or key blocks kvb+1..min(qb, n_kvb-1) (descending order)
+        const int before = p.kv_reverse ? min(qb, n_kvb - 1) - kvb : kvb;
+        turn = wait_counter(ticket, before, abort, status);
         fence_proxy_async_global();
       }
       if (lane == 0 && turn) {

@@ -30,6 +30,7 @@ struct BwdParams {
   int causal;
   int dq_mode;
   int max_q_blocks;    // query blocks of the longest query sequence
+  int kv_reverse;      // 1: blockIdx.x counts key blocks from the last one down
   float scale;         // softmax scale (multiplies dK in the epilogue)
   float scale_log2;    // scale * log2(e)
 };
