@@ -118,6 +118,16 @@ def backward_head(q, k, v, o, do, m, l, scale: float, causal: bool):
     return dq, dk, dv, D
 
 
+def _kv_head(h: int, hq: int, hkv: int) -> int:
+    """Key/value head used by query head h when hq query heads share hkv
+    key/value heads in equal consecutive groups (grouped-query attention,
+    the JAX cuDNN wrapper's q_N != kv_N case; hkv = hq is plain multi-head,
+    hkv = 1 is multi-query)."""
+    if hq % hkv != 0:
+        raise ValueError(f"query heads ({hq}) must be a multiple of key/value heads ({hkv})")
+    return h // (hq // hkv)
+
+
 def forward_packed(q, k, v, cu_q, cu_kv, scale: float, causal: bool,
                    heads_subset=None):
     """Forward statistics over a packed batch ``[total, H, d]``.
@@ -125,12 +135,14 @@ def forward_packed(q, k, v, cu_q, cu_kv, scale: float, causal: bool,
     cu_q / cu_kv are the cumulative offsets (``actual_q`` / ``actual_kv``,
     section 3).  Rows outside every sequence are left at O = 0, m = -inf,
     l = 0.  ``heads_subset`` restricts the work to a list of (b, h) pairs.
+    K and V may have fewer heads than Q (grouped-query attention).
     Returns float64 arrays O [total_q, H, d], m and l [total_q, H].
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     cu_q = np.asarray(cu_q, dtype=np.int64)
     cu_kv = np.asarray(cu_kv, dtype=np.int64)
     total_q, H, d = q.shape
+    Hkv = k.shape[1]
     o = np.zeros((total_q, H, v.shape[2]))
     m = np.full((total_q, H), -np.inf)
     l = np.zeros((total_q, H))
@@ -139,7 +151,8 @@ def forward_packed(q, k, v, cu_q, cu_kv, scale: float, causal: bool,
     for b, h in units:
         qs, qe = cu_q[b], cu_q[b + 1]
         ks, ke = cu_kv[b], cu_kv[b + 1]
-        ob, mb, lb = forward_head(q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], scale, causal)
+        hk = _kv_head(h, H, Hkv)
+        ob, mb, lb = forward_head(q[qs:qe, h], k[ks:ke, hk], v[ks:ke, hk], scale, causal)
         o[qs:qe, h], m[qs:qe, h], l[qs:qe, h] = ob, mb, lb
     return o, m, l
 
@@ -148,14 +161,17 @@ def backward_packed(q, k, v, o, do, m, l, cu_q, cu_kv, scale: float,
                     causal: bool, heads_subset=None):
     """Backward over a packed batch from the given (O, m, l).
 
-    Returns float64 dQ [total_q,H,d], dK and dV [total_kv,H,d] and
+    Returns float64 dQ [total_q,H,d], dK and dV [total_kv,Hkv,d] and
     D [total_q,H].  Rows outside every sequence (padding) are exactly 0.
+    With grouped-query attention (K, V with Hkv < H heads) the gradient of a
+    shared key/value head is the sum over the query heads of its group.
     """
     q, k, v, o, do = (_f64(t) for t in (q, k, v, o, do))
     m, l = _f64(m), _f64(l)
     cu_q = np.asarray(cu_q, dtype=np.int64)
     cu_kv = np.asarray(cu_kv, dtype=np.int64)
     H = q.shape[1]
+    Hkv = k.shape[1]
     dq = np.zeros(q.shape)
     dk = np.zeros(k.shape)
     dv = np.zeros(v.shape)
@@ -165,7 +181,10 @@ def backward_packed(q, k, v, o, do, m, l, cu_q, cu_kv, scale: float,
     for b, h in units:
         qs, qe = cu_q[b], cu_q[b + 1]
         ks, ke = cu_kv[b], cu_kv[b + 1]
-        r = backward_head(q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], o[qs:qe, h],
+        hk = _kv_head(h, H, Hkv)
+        r = backward_head(q[qs:qe, h], k[ks:ke, hk], v[ks:ke, hk], o[qs:qe, h],
                           do[qs:qe, h], m[qs:qe, h], l[qs:qe, h], scale, causal)
-        dq[qs:qe, h], dk[ks:ke, h], dv[ks:ke, h], D[qs:qe, h] = r
+        dq[qs:qe, h], D[qs:qe, h] = r[0], r[3]
+        dk[ks:ke, hk] += r[1]
+        dv[ks:ke, hk] += r[2]
     return dq, dk, dv, D

@@ -62,10 +62,15 @@ class Case:
     pad_q: int = 0      # NaN rows appended after the last query row
     pad_kv: int = 0     # NaN rows appended after the last key row
     scale: float | None = None
+    heads_kv: int | None = None   # key/value heads (grouped-query attention); None = heads
 
     @property
     def batch(self) -> int:
         return len(self.q_lens)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.heads if self.heads_kv is None else self.heads_kv
 
     @property
     def softmax_scale(self) -> float:
@@ -98,10 +103,10 @@ class Case:
 
     def tensors(self):
         """Q, K, V, dO as CPU bf16 tensors, padding rows set to NaN."""
-        H, d = self.heads, self.head_dim
+        H, Hkv, d = self.heads, self.kv_heads, self.head_dim
         q = bf16_normal((self.total_q, H, d), self.seed, 0)
-        k = bf16_normal((self.total_kv, H, d), self.seed, 1)
-        v = bf16_normal((self.total_kv, H, d), self.seed, 2)
+        k = bf16_normal((self.total_kv, Hkv, d), self.seed, 1)
+        v = bf16_normal((self.total_kv, Hkv, d), self.seed, 2)
         do = bf16_normal((self.total_q, H, d), self.seed, 3)
         nq, nkv = int(self.cu_q[-1]), int(self.cu_kv[-1])
         for t, n in ((q, nq), (do, nq), (k, nkv), (v, nkv)):

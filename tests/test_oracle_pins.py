@@ -251,3 +251,49 @@ def test_heads_subset_matches_full():
         rows = slice(cu[b], cu[b + 1])
         for a, bb in zip(full[:3], part[:3]):
             np.testing.assert_array_equal(a[rows, h], bb[rows, h])
+
+
+# ---------------------------------------------------------------- grouped-query attention
+@pytest.mark.parametrize("hq,hkv,causal", [(4, 2, False), (4, 2, True), (3, 1, True)])
+def test_gqa_finite_differences(hq, hkv, causal):
+    """Query heads sharing a key/value head: finite differences of
+    L = sum(O * dO) through the packed forward pin dK and dV of the shared
+    head (sums over the group) as well as dQ."""
+    d, scale = 3, 0.6
+    cu_q = np.array([0, 4, 7], dtype=np.int32)
+    cu_kv = np.array([0, 5, 8], dtype=np.int32)
+    q, k, v = rnd((7, hq, d), 61), rnd((8, hkv, d), 62), rnd((8, hkv, d), 63)
+    do = rnd((7, hq, d), 64)
+    o, m, l = forward_packed(q, k, v, cu_q, cu_kv, scale, causal)
+    dq, dk, dv, _ = backward_packed(q, k, v, o, do, m, l, cu_q, cu_kv, scale, causal)
+
+    def loss(q_, k_, v_):
+        o_, _, _ = forward_packed(q_, k_, v_, cu_q, cu_kv, scale, causal)
+        return float((o_ * do).sum())
+
+    h = 1e-6
+    for t, g, slot in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(t)
+        for idx in np.ndindex(t.shape):
+            tp, tm = t.copy(), t.copy()
+            tp[idx] += h
+            tm[idx] -= h
+            ap, am = [q, k, v], [q, k, v]
+            ap[slot], am[slot] = tp, tm
+            num[idx] = (loss(*ap) - loss(*am)) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-7)
+
+
+def test_gqa_with_one_group_is_multi_head():
+    """hkv = hq reduces to the per-head definition exactly."""
+    H, d, scale = 3, 4, 0.5
+    cu = np.array([0, 6], dtype=np.int32)
+    q, k, v, do = (rnd((6, H, d), s) for s in (70, 71, 72, 73))
+    o, m, l = forward_packed(q, k, v, cu, cu, scale, True)
+    dq, dk, dv, _ = backward_packed(q, k, v, o, do, m, l, cu, cu, scale, True)
+    for h in range(H):
+        oh, mh, lh = forward_head(q[:, h], k[:, h], v[:, h], scale, True)
+        r = backward_head(q[:, h], k[:, h], v[:, h], oh, do[:, h], mh, lh, scale, True)
+        np.testing.assert_array_equal(dq[:, h], r[0])
+        np.testing.assert_array_equal(dk[:, h], r[1])
+        np.testing.assert_array_equal(dv[:, h], r[2])
