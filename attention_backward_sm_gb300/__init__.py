@@ -87,6 +87,17 @@ def fa_fwd_stats(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, c
                               int(bool(causal)), float(scale), _stream(stream)))
 
 
+def fa_fwd_stats_gqa(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
+                     stream=None):
+    """fa_fwd_stats with k, v carrying k.shape[1] key/value heads."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv, heads_kv = int(k.shape[0]), int(k.shape[1])
+    _check(lib().fa_fwd_stats_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(m), _ptr(l), _ptr(cu_q_dev),
+                                  _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1, total_q, total_kv, heads, heads_kv,
+                                  dim, int(bool(causal)), float(scale), _stream(stream)))
+
+
 def fa_bwd_preprocess(o, do, D, dq_acc, stream=None):
     total_q, heads, dim = _shape(o)
     _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(D), _ptr(dq_acc), total_q, heads, dim,
@@ -112,6 +123,19 @@ def fa_bwd(q, k, v, do, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host,
                         _ptr(dv), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1, total_q, total_kv,
                         heads, dim, int(bool(causal)), float(scale), int(dq_mode), _ptr(workspace), ws_bytes,
                         _stream(stream)))
+
+
+def fa_bwd_gqa(q, k, v, do, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool,
+               scale: float, dq_mode: int = FA_DQ_ATOMIC, workspace=None, stream=None):
+    """fa_bwd with k, v, dk, dv carrying k.shape[1] key/value heads."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv, heads_kv = int(k.shape[0]), int(k.shape[1])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(m), _ptr(l), _ptr(D), _ptr(dq_acc),
+                            _ptr(dk), _ptr(dv), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1,
+                            total_q, total_kv, heads, heads_kv, dim, int(bool(causal)), float(scale), int(dq_mode),
+                            _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def fa_bwd_dq_finalize(dq_acc, dq, scale: float, stream=None):
@@ -141,7 +165,7 @@ def forward_stats(q, k, v, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: b
     o = torch.zeros_like(q)
     m = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
     l = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
-    fa_fwd_stats(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal, scale, stream)
+    fa_fwd_stats_gqa(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal, scale, stream)
     return o, m, l
 
 
@@ -158,14 +182,15 @@ class Workspace:
 
 def backward(q, k, v, o, do, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
              dq_mode: int = FA_DQ_ATOMIC, out=None, work: Workspace | None = None, stream=None):
-    """preprocess -> fa_bwd -> finalize on one stream; returns (dq, dk, dv)."""
+    """preprocess -> fa_bwd -> finalize on one stream; returns (dq, dk, dv).
+    k and v may have fewer heads than q (grouped-query attention)."""
     if work is None:
         work = Workspace(q, cu_q_host, cu_kv_host, causal, dq_mode)
     if out is None:
         out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     dq, dk, dv = out
     fa_bwd_preprocess(o, do, work.D, work.dq_acc, stream)
-    fa_bwd(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal,
-           scale, dq_mode, work.ws, stream)
+    fa_bwd_gqa(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal,
+               scale, dq_mode, work.ws, stream)
     fa_bwd_dq_finalize(work.dq_acc, dq, scale, stream)
     return dq, dk, dv

@@ -68,6 +68,13 @@ int check_shape(int batch, int total_q, int total_kv, int heads, int head_dim) {
   return FA_OK;
 }
 
+int check_groups(int heads, int heads_kv) {
+  if (heads_kv < 1 || heads % heads_kv != 0)
+    return fail(FA_ERR_INVALID_ARG, "query heads (%d) must be a positive multiple of key/value heads (%d)", heads,
+                heads_kv);
+  return FA_OK;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -129,12 +136,13 @@ extern "C" {
 
 const char* fa_last_error(void) { return g_err; }
 
-int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
-                 const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
-                 const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int head_dim, int causal,
-                 float scale, fa_stream_t stream) {
+int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
+                     const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
+                     const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int heads_kv,
+                     int head_dim, int causal, float scale, fa_stream_t stream) {
   int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
   if (rc) return rc;
+  if ((rc = check_groups(heads, heads_kv))) return rc;
   if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
   if (!isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
   int max_q = 0, max_kv = 0;
@@ -154,11 +162,20 @@ int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* 
   p.cu_q = cu_q_dev;
   p.cu_kv = cu_kv_dev;
   p.heads = heads;
+  p.heads_kv = heads_kv;
   p.causal = causal;
   p.scale = scale;
   cudaError_t e = fa::launch_fwd_stats(p, head_dim, batch, (max_q + 63) / 64, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fwd_stats launch");
   return ok();
+}
+
+int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
+                 const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
+                 const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int head_dim, int causal,
+                 float scale, fa_stream_t stream) {
+  return fa_fwd_stats_gqa(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q, total_kv,
+                          heads, heads, head_dim, causal, scale, stream);
 }
 
 int fa_bwd_preprocess(const fa_bf16* o, const fa_bf16* dout, float* D, float* dq_acc, int total_q, int heads,
@@ -201,13 +218,14 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   return ((n * 4 + 255) / 256) * 256;
 }
 
-int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m, const float* l,
-           const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
-           const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads,
-           int head_dim, int causal, float scale, int dq_mode, void* workspace, size_t workspace_bytes,
-           fa_stream_t stream) {
+int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
+               const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
+               const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
+               int total_kv, int heads, int heads_kv, int head_dim, int causal, float scale, int dq_mode,
+               void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
   if (rc) return rc;
+  if ((rc = check_groups(heads, heads_kv))) return rc;
   if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
   if (dq_mode != FA_DQ_ATOMIC && dq_mode != FA_DQ_DETERMINISTIC)
     return fail(FA_ERR_INVALID_ARG, "dq_mode must be 0 or 1, got %d", dq_mode);
@@ -231,11 +249,11 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
   if ((rc = check_device())) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (total_kv > kv_used) {
-    const long long row_bytes = static_cast<long long>(heads) * head_dim * 2;
-    cudaError_t e = fa::launch_zero_fill(dk + static_cast<long long>(kv_used) * heads * head_dim,
+    const long long row_bytes = static_cast<long long>(heads_kv) * head_dim * 2;
+    cudaError_t e = fa::launch_zero_fill(dk + static_cast<long long>(kv_used) * heads_kv * head_dim,
                                          (total_kv - kv_used) * row_bytes, s);
     if (e == cudaSuccess)
-      e = fa::launch_zero_fill(dv + static_cast<long long>(kv_used) * heads * head_dim,
+      e = fa::launch_zero_fill(dv + static_cast<long long>(kv_used) * heads_kv * head_dim,
                                (total_kv - kv_used) * row_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "padding zero fill");
   }
@@ -246,10 +264,13 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
   // then stands in as a valid address for the (unused) query maps.
   const void* qbase = max_q > 0 ? static_cast<const void*>(q) : static_cast<const void*>(k);
   const void* dobase = max_q > 0 ? static_cast<const void*>(dout) : static_cast<const void*>(k);
-  if ((rc = make_map(&p.tm_q, qbase, max_q > 0 ? total_q : total_kv, heads, head_dim, "q"))) return rc;
-  if ((rc = make_map(&p.tm_k, k, total_kv, heads, head_dim, "k"))) return rc;
-  if ((rc = make_map(&p.tm_v, v, total_kv, heads, head_dim, "v"))) return rc;
-  if ((rc = make_map(&p.tm_do, dobase, max_q > 0 ? total_q : total_kv, heads, head_dim, "dout"))) return rc;
+  if ((rc = make_map(&p.tm_q, qbase, max_q > 0 ? total_q : total_kv, max_q > 0 ? heads : heads_kv, head_dim, "q")))
+    return rc;
+  if ((rc = make_map(&p.tm_k, k, total_kv, heads_kv, head_dim, "k"))) return rc;
+  if ((rc = make_map(&p.tm_v, v, total_kv, heads_kv, head_dim, "v"))) return rc;
+  if ((rc = make_map(&p.tm_do, dobase, max_q > 0 ? total_q : total_kv, max_q > 0 ? heads : heads_kv, head_dim,
+                     "dout")))
+    return rc;
   if (max_q > 0 && (rc = make_map(&p.tm_dq, dq_acc, total_q, heads, head_dim, "dq_acc", true))) return rc;
   p.m = m;
   p.l = l;
@@ -260,6 +281,7 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
   p.cu_q = cu_q_dev;
   p.cu_kv = cu_kv_dev;
   p.heads = heads;
+  p.heads_kv = heads_kv;
   p.causal = causal;
   p.dq_mode = dq_mode;
   p.max_q_blocks = (max_q + 127) / 128;
@@ -274,6 +296,16 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
   cudaError_t e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, s);
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
   return ok();
+}
+
+int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m, const float* l,
+           const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+           const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads,
+           int head_dim, int causal, float scale, int dq_mode, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream) {
+  return fa_bwd_gqa(q, k, v, dout, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch,
+                    total_q, total_kv, heads, heads, head_dim, causal, scale, dq_mode, workspace, workspace_bytes,
+                    stream);
 }
 
 int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads, int head_dim, float scale,

@@ -250,8 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   // launched before it (see the dQ write-back).
   const int kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
                                : static_cast<int>(blockIdx.x);
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int H = p.heads;
+  // Grouped-query attention: the CTA owns key/value head hk, shared by the
+  // G query heads hk*G .. hk*G+G-1, and sweeps the query blocks of each of
+  // them in turn; dK and dV accumulate over the whole group in TMEM.
+  const int hk = blockIdx.y, b = blockIdx.z;
+  const int H = p.heads;                            // query heads
+  const int G = p.heads / p.heads_kv;
   const int q_start = p.cu_q[b], s1 = p.cu_q[b + 1] - q_start;
   const int kv_start = p.cu_kv[b], s2 = p.cu_kv[b + 1] - kv_start;
   if (kvb * BM >= s2) return;                       // CTA-uniform, before any barrier
@@ -262,10 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   const int kv_valid = min(BM, s2 - kvb * BM);
   const int n_qb = (s1 + BN - 1) / BN;
   const int qb0 = p.causal ? kvb : 0;               // top-left mask: query block >= key block
-  const int n_it = max(0, n_qb - qb0);
+  const int n_qit = max(0, n_qb - qb0);             // query blocks per query head
+  const int n_it = G * n_qit;                       // iterations of the sweep
   const int n_kvb = (s2 + BM - 1) / BM;
-  auto qb_of = [&](int k) { return qb0 + k; };
-  const long long rs = static_cast<long long>(H) * D;   // row stride (elements)
+  const int nq_div = max(1, n_qit);                 // divisor that stays valid when there is no work
+  auto qb_of = [&](int k) { return qb0 + k % nq_div; };
+  auto hq_of = [&](int k) { return hk * G + k / nq_div; };
+  const long long rs_kv = static_cast<long long>(p.heads_kv) * D;   // key-side row stride (elements)
 
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC + 4);
@@ -319,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         tma_prefetch_desc(&p.tm_do);
         mbar_arrive_expect_tx(bar(B_KV_FULL), 2 * L::TILE);
         for (int c = 0; c < L::NCH; ++c) {
-          tma_load_2d(sbase + L::K + c * CHUNK, &p.tm_k, h * D + c * 64, kv_start + kvb * BM, bar(B_KV_FULL));
-          tma_load_2d(sbase + L::V + c * CHUNK, &p.tm_v, h * D + c * 64, kv_start + kvb * BM, bar(B_KV_FULL));
+          tma_load_2d(sbase + L::K + c * CHUNK, &p.tm_k, hk * D + c * 64, kv_start + kvb * BM, bar(B_KV_FULL));
+          tma_load_2d(sbase + L::V + c * CHUNK, &p.tm_v, hk * D + c * 64, kv_start + kvb * BM, bar(B_KV_FULL));
         }
       }
       __syncwarp();
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           b[j] = 1.f;
           c[j] = 0.f;
           if (k < n_it && r < q_valid) {
-            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + h;
+            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
             a[j] = __ldg(p.m + idx);
             b[j] = __ldg(p.l + idx);
             c[j] = __ldg(p.D + idx);
@@ -371,13 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         load_stats(k + 1, nm, nl, nd);
         const int qb = qb_of(k);
+        const int hq = hq_of(k);
         const int q_row0 = q_start + qb * BN;
         const int q_valid = min(BN, s1 - qb * BN);
         if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), L::TILE);
           for (int c = 0; c < L::NCH; ++c)
-            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, h * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
+            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, hq * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
         }
         pend_q = s;
         par_q = (k >> 1) & 1;
@@ -398,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_DO_FULL0 + s), L::TILE);
           for (int c = 0; c < L::NCH; ++c)
-            tma_load_2d(sbase + L::DO + s * L::TILE + c * CHUNK, &p.tm_do, h * D + c * 64, q_row0,
+            tma_load_2d(sbase + L::DO + s * L::TILE + c * CHUNK, &p.tm_do, hq * D + c * 64, q_row0,
                         bar(B_DO_FULL0 + s));
         }
         pend_do = s;
@@ -576,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const int kv_row = kv_start + kvb * BM + r;
     uint16_t* out = (wg == 0) ? p.dv : p.dk;
     const float mul = (wg == 0) ? 1.f : p.scale;
-    uint8_t* dst = reinterpret_cast<uint8_t*>(out + static_cast<long long>(kv_row) * rs + h * D);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(out + static_cast<long long>(kv_row) * rs_kv + hk * D);
     if (n_it == 0) {
       if (r < kv_valid)
         for (int c = 0; c < D; c += 8) st_global_v4(dst + c * 2, 0u, 0u, 0u, 0u);
@@ -631,9 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     for (int k = 0; k < n_it; ++k) {
       const int s = k & 1;
       const int qb = qb_of(k);
+      const int hq = hq_of(k);
       const int y = q_start + qb * BN + quarter * 32;
       const uint32_t slot_b = sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
-      int* ticket = det ? p.tickets + (static_cast<long long>(b * H + h) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
+      int* ticket = det ? p.tickets + (static_cast<long long>(b * H + hq) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
       if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
       tc_fence_after();
       uint32_t va[32], vb[32], vc[32], vd[32];
@@ -660,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         fence_proxy_async_global();
       }
       if (lane == 0 && turn) {
-        tma_reduce_add_2d(&p.tm_dq, slot_a, h * D + 0, y);
-        if (BPH == 2) tma_reduce_add_2d(&p.tm_dq, slot_a + 4096, h * D + 32, y);
+        tma_reduce_add_2d(&p.tm_dq, slot_a, hq * D + 0, y);
+        if (BPH == 2) tma_reduce_add_2d(&p.tm_dq, slot_a + 4096, hq * D + 32, y);
         bulk_commit();
         issued = true;
       }
@@ -675,10 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       __syncwarp();
       if (lane == 0 && turn) {
         if (BPH == 2) {
-          tma_reduce_add_2d(&p.tm_dq, slot_b, h * D + 64, y);
-          tma_reduce_add_2d(&p.tm_dq, slot_b + 4096, h * D + 96, y);
+          tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 64, y);
+          tma_reduce_add_2d(&p.tm_dq, slot_b + 4096, hq * D + 96, y);
         } else {
-          tma_reduce_add_2d(&p.tm_dq, slot_b, h * D + 32, y);
+          tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 32, y);
         }
         bulk_commit();
         asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
@@ -714,7 +723,7 @@ cudaError_t launch_d(const BwdParams& p, int batch, int max_kv_blocks, cudaStrea
   static_assert(bytes <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(max_kv_blocks, p.heads, batch);
+  dim3 grid(max_kv_blocks, p.heads_kv, batch);
   bwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);
   return cudaGetLastError();
 }

@@ -4,7 +4,8 @@
 // (section 3.1 step 2) defines P from exactly these m and l; section 5
 // names the online-softmax forward skeleton as their producer.
 //
-// One CTA computes a 64-row query block of one (sequence, head) with an
+// One CTA computes a 64-row query block of one (sequence, query head; the
+// key/value head is shared by a group of query heads) with an
 // online softmax over 64-row key blocks, on the CUDA cores in fp32 (every
 // product and sum in fp32, P kept in fp32).  256 threads: thread t owns
 // query rows 4*(t/16) .. +3; in the score phase it owns key columns
@@ -43,7 +44,9 @@ __global__ void __launch_bounds__(256) fwd_stats_kernel(const FwdParams p) {
   const int k0 = p.cu_kv[b], s2 = p.cu_kv[b + 1] - k0;
   if (qb * BQ >= s1) return;
   const int H = p.heads;
-  const long long rs = static_cast<long long>(H) * D;   // row stride in elements
+  const long long rs = static_cast<long long>(H) * D;   // query-side row stride in elements
+  const long long rs_kv = static_cast<long long>(p.heads_kv) * D;
+  const int hk = h / (H / p.heads_kv);                   // key/value head of this query head
   const int tid = threadIdx.x;
   const int rg = tid >> 4, cg = tid & 15;
   constexpr int OC = D / 16;   // output columns per thread
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(256) fwd_stats_kernel(const FwdParams p) {
       const int r = e / D, c = e % D;
       const int kj = kb * BK + r;
       const bool ok = kj < s2;
-      const long long g = (k0 + kj) * rs + h * D + c;
+      const long long g = (k0 + kj) * rs_kv + hk * D + c;
       kT[c * LD + r] = ok ? bf2f(p.k[g]) : 0.f;
       vs[r * D + c] = ok ? bf2f(p.v[g]) : 0.f;
     }

@@ -26,7 +26,8 @@ struct BwdParams {
   const int32_t* cu_q;
   const int32_t* cu_kv;
   int* tickets;        // deterministic mode: one counter per (batch, head, query block, 32-row quarter)
-  int heads;
+  int heads;           // query heads
+  int heads_kv;        // key/value heads (heads is a multiple of it)
   int causal;
   int dq_mode;
   int max_q_blocks;    // query blocks of the longest query sequence
@@ -52,7 +53,8 @@ struct FwdParams {
   float* l;
   const int32_t* cu_q;
   const int32_t* cu_kv;
-  int heads;
+  int heads;           // query heads
+  int heads_kv;        // key/value heads (heads is a multiple of it)
   int causal;
   float scale;
 };

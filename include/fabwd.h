@@ -77,6 +77,19 @@ int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
                  int batch, int total_q, int total_kv, int heads, int head_dim,
                  int causal, float scale, fa_stream_t stream);
 
+/* fa_fwd_stats for grouped-query attention: k and v have heads_kv heads
+ * ([total_kv, heads_kv, d]); query head h uses key/value head
+ * h / (heads / heads_kv) (consecutive groups; the JAX cuDNN wrapper's
+ * q_N != kv_N case, page 3 `_dot_product_attention_bwd_cuda_lowering`).
+ * heads must be a positive multiple of heads_kv.  fa_fwd_stats is this
+ * call with heads_kv = heads. */
+int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
+                     fa_bf16* o, float* m, float* l,
+                     const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+                     const int32_t* cu_q_host, const int32_t* cu_kv_host,
+                     int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
+                     int causal, float scale, fa_stream_t stream);
+
 /* Backward preprocess (section 3.1 step 4; section 4.2 row "D"):
  * D[r, h] = sum_k float(O[r,h,k]) * float(dO[r,h,k]) for every row
  * r < total_q, and dq_acc[r, h, :] = 0 (float32 accumulator of
@@ -111,6 +124,23 @@ int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* 
            int batch, int total_q, int total_kv, int heads, int head_dim,
            int causal, float scale, int dq_mode,
            void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* fa_bwd for grouped-query attention: q, dout, m, l, D, dq_acc have heads
+ * query heads; k, v, dk, dv have heads_kv heads ([total_kv, heads_kv, d]);
+ * query head h attends with key/value head h / (heads / heads_kv).  The
+ * gradients of a shared key/value head are the sums over its query heads:
+ * one CTA per (sequence, key/value head, key block) sweeps the query blocks
+ * of every query head of the group, accumulating dK and dV on chip.
+ * fa_bwd is this call with heads_kv = heads; the workspace size is that of
+ * fa_bwd with `heads` query heads. */
+int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout,
+               const float* m, const float* l, const float* D,
+               float* dq_acc, fa_bf16* dk, fa_bf16* dv,
+               const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+               const int32_t* cu_q_host, const int32_t* cu_kv_host,
+               int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
+               int causal, float scale, int dq_mode,
+               void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* dQ write-back (section 3, V2 applies scale to dq; section 4.2 row dQ:
  * fp32 accumulate, then bf16): dq[e] = bf16_rne(scale * dq_acc[e]) for all

@@ -125,13 +125,25 @@ def check_case(prep: Prepared, out=None, dq_mode=0):
         for name, g, r, z in zip(("dq", "dk", "dv"), got, ref[:3], (zq, zk, zk)):
             errs[name] = compare(name, g, r, np.broadcast_to(z[:, None, None], g.shape))
     else:
+        # dQ per checked (sequence, query head); dK/dV per (sequence, key/value
+        # head) whose whole group of query heads is checked (with grouped-query
+        # attention a key/value head's gradient sums over its group).
+        G = case.heads // case.kv_heads
         for b, h in units:
             qr = slice(int(case.cu_q[b]), int(case.cu_q[b + 1]))
+            gg = got[0][qr, h]
+            errs[f"dq[{b},{h}]"] = compare(f"dq[b={b},h={h}]", gg, ref[0][qr, h],
+                                           np.broadcast_to(zq[qr][:, None], gg.shape))
+        checked = set(units)
+        groups = sorted({(b, h // G) for b, h in units
+                         if all((b, h // G * G + i) in checked for i in range(G))})
+        assert groups, "no complete group of query heads among the checked units"
+        for b, hk in groups:
             kr = slice(int(case.cu_kv[b]), int(case.cu_kv[b + 1]))
-            for name, g, r, rows, z in zip(("dq", "dk", "dv"), got, ref[:3], (qr, kr, kr), (zq, zk, zk)):
-                gg = g[rows, h]
-                errs[f"{name}[{b},{h}]"] = compare(f"{name}[b={b},h={h}]", gg, r[rows, h],
-                                                   np.broadcast_to(z[rows][:, None], gg.shape))
+            for name, g, r in zip(("dk", "dv"), got[1:], ref[1:3]):
+                gg = g[kr, hk]
+                errs[f"{name}[{b},{hk}]"] = compare(f"{name}[b={b},hkv={hk}]", gg, r[kr, hk],
+                                                    np.broadcast_to(zk[kr][:, None], gg.shape))
     # structural zeros hold for every head, checked or not
     for g, z in ((got[0], zq), (got[1], zk), (got[2], zk)):
         assert np.all(g[z] == 0), "non-zero gradient in a padding row or a row no query/key reaches"

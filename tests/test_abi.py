@@ -27,7 +27,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     syms = declared_symbols()
-    for name in ("fa_fwd_stats", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_dq_finalize", "fa_bwd_workspace_size",
+    for name in ("fa_fwd_stats", "fa_fwd_stats_gqa", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_gqa",
+                 "fa_bwd_dq_finalize", "fa_bwd_workspace_size",
                  "fa_check_device_status", "fa_last_error"):
         assert name in syms
 
@@ -82,3 +83,21 @@ def test_workspace_size(lib):
     assert n >= 2 * 4 * 4 * 4 and n % 256 == 0               # one int32 per (b, h, query block)
     assert lib.fa_bwd_workspace_size(hp, hp, 2, 4, 128, 1, 5) == 0
     assert b"dq_mode" in lib.fa_last_error()
+
+
+def test_gqa_host_argument_checks(lib):
+    """fa_bwd_gqa / fa_fwd_stats_gqa reject head counts that do not form
+    equal groups before touching the device."""
+    cu = _offsets(0, 10, 30)
+    hp = cu.ctypes.data_as(ctypes.c_void_p)
+    p = ctypes.c_void_p(16)
+    for heads, heads_kv in ((6, 4), (4, 0), (4, -2), (2, 4)):
+        rc = lib.fa_bwd_gqa(p, p, p, p, p, p, p, p, p, p, p, p, hp, hp, 2, 30, 30, heads, heads_kv, 128, 0, 0.1, 0,
+                            None, 0, None)
+        assert rc == 1, (heads, heads_kv)
+        assert b"multiple" in lib.fa_last_error()
+        rc = lib.fa_fwd_stats_gqa(p, p, p, p, p, p, p, p, hp, hp, 2, 30, 30, heads, heads_kv, 128, 0, 0.1, None)
+        assert rc == 1, (heads, heads_kv)
+    # shape checks still come first
+    assert lib.fa_bwd_gqa(p, p, p, p, p, p, p, p, p, p, p, p, hp, hp, 2, 30, 30, 4, 2, 96, 0, 0.1, 0,
+                          None, 0, None) == 2
