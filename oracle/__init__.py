@@ -12,4 +12,5 @@ from .attention import (  # noqa: F401
     backward_packed,
     rowsum_o_do,
     masked_scores,
+    visible,
 )

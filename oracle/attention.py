@@ -28,6 +28,16 @@ Readings where the pages are silent (each also listed in the design notes):
     step 4, section 4.2 row "D"), not from P @ V.
   * The causal mask is top-left aligned: query i (local index) sees key j
     iff j <= i.  Masked entries have P = 0 exactly.
+  * Bottom-right causal (not defined by the pages; the usual alignment of
+    the causal diagonal with the last key): query i sees key j iff
+    j <= i + (s2 - s1).
+  * Sliding window of length W (JAX ``dot_product_attention``,
+    ``sliding_window_length``: each token sees the left window
+    (pos - W, pos]): query i sees key j iff i + off - W < j <= i + off,
+    off = 0 (top-left) or s2 - s1 (bottom-right).  The window carries the
+    causal upper bound, so it is only defined together with a causal mask.
+  * A row that sees no key (no keys at all, or every key masked) has
+    m = -inf, l = 0, O = 0 and dQ = 0.
   * A row with no keys (s2 = 0) has m = -inf, l = 0, O = 0, dQ = 0.
   * No bf16 rounding of P or dS is emulated: the oracle is the exact
     gradient of the stated inputs.
@@ -46,40 +56,62 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def masked_scores(q, k, scale: float, causal: bool) -> np.ndarray:
+def visible(s1: int, s2: int, causal: bool, window: int = 0, bottom_right: bool = False) -> np.ndarray:
+    """Boolean [s1, s2] matrix: may query i attend to key j.
+
+    Non-causal: every pair.  Causal: j <= i + off, off = 0 for the top-left
+    alignment and s2 - s1 for the bottom-right one.  A sliding window of
+    length W > 0 (JAX ``dot_product_attention`` ``sliding_window_length``,
+    the left window (pos - W, pos]) further requires j > i + off - W."""
+    if window < 0:
+        raise ValueError("window must be >= 0")
+    if (window > 0 or bottom_right) and not causal:
+        raise ValueError("a sliding window or the bottom-right alignment needs a causal mask")
+    i = np.arange(s1)[:, None]
+    j = np.arange(s2)[None, :]
+    if not causal:
+        return np.ones((s1, s2), dtype=bool)
+    off = s2 - s1 if bottom_right else 0
+    vis = j <= i + off
+    if window > 0:
+        vis &= j > i + off - window
+    return vis
+
+
+def masked_scores(q, k, scale: float, causal: bool, window: int = 0, bottom_right: bool = False) -> np.ndarray:
     """X = scale * Q K^T with masked entries set to -inf.
 
-    Section 3.1 steps 1-2 (S = Q K^T, then S * scale); causal masking
-    follows the top-left reading (key j visible to query i iff j <= i)."""
+    Section 3.1 steps 1-2 (S = Q K^T, then S * scale); the mask is
+    ``visible`` (top-left causal unless told otherwise)."""
     q = _f64(q)
     k = _f64(k)
     x = scale * (q @ k.T)
-    if causal:
-        s1, s2 = x.shape
-        i = np.arange(s1)[:, None]
-        j = np.arange(s2)[None, :]
-        x = np.where(j <= i, x, -np.inf)
-    return x
+    return np.where(visible(x.shape[0], x.shape[1], causal, window, bottom_right), x, -np.inf)
 
 
-def forward_head(q, k, v, scale: float, causal: bool):
+def forward_head(q, k, v, scale: float, causal: bool, window: int = 0, bottom_right: bool = False):
     """Forward statistics of one head: (O, m, l), all float64.
 
     m_i = max_j X_ij, l_i = sum_j exp(X_ij - m_i), P = exp(X - m) / l,
     O = P V.  These are the statistics the SK-16 backward consumes
     (section 3.1 step 2; section 5 says the forward skeleton supplies them).
+    Rows that see no key keep m = -inf, l = 0, O = 0.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     s1, d = q.shape
     s2 = k.shape[0]
+    o = np.zeros((s1, v.shape[1]))
+    m = np.full(s1, -np.inf)
+    l = np.zeros(s1)
     if s2 == 0:
-        return (np.zeros((s1, v.shape[1])), np.full(s1, -np.inf), np.zeros(s1))
-    x = masked_scores(q, k, scale, causal)
-    m = x.max(axis=1)
-    e = np.exp(x - m[:, None])
-    l = e.sum(axis=1)
-    p = e / l[:, None]
-    o = p @ v
+        return o, m, l
+    x = masked_scores(q, k, scale, causal, window, bottom_right)
+    rows = np.isfinite(x).any(axis=1)
+    x = x[rows]
+    m[rows] = x.max(axis=1)
+    e = np.exp(x - m[rows][:, None])
+    l[rows] = e.sum(axis=1)
+    o[rows] = (e / l[rows][:, None]) @ v
     return o, m, l
 
 
@@ -88,7 +120,7 @@ def rowsum_o_do(o, do) -> np.ndarray:
     return (_f64(o) * _f64(do)).sum(axis=1)
 
 
-def backward_head(q, k, v, o, do, m, l, scale: float, causal: bool):
+def backward_head(q, k, v, o, do, m, l, scale: float, causal: bool, window: int = 0, bottom_right: bool = False):
     """Gradients of one head from the given forward statistics.
 
     Follows section 3.1 in its order:
@@ -108,8 +140,11 @@ def backward_head(q, k, v, o, do, m, l, scale: float, causal: bool):
     D = rowsum_o_do(o, do)
     if s1 == 0 or s2 == 0:
         return (np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), D)
-    x = masked_scores(q, k, scale, causal)
-    p = np.exp(x - m[:, None]) / l[:, None]
+    x = masked_scores(q, k, scale, causal, window, bottom_right)
+    # P is 0 at masked entries; rows that see no key (l = 0) are all 0
+    rows = l > 0
+    p = np.zeros_like(x)
+    p[rows] = np.exp(x[rows] - m[rows][:, None]) / l[rows][:, None]
     dp = do @ v.T
     ds = p * (dp - D[:, None])
     dk = scale * (ds.T @ q)
@@ -129,7 +164,7 @@ def _kv_head(h: int, hq: int, hkv: int) -> int:
 
 
 def forward_packed(q, k, v, cu_q, cu_kv, scale: float, causal: bool,
-                   heads_subset=None):
+                   heads_subset=None, window: int = 0, bottom_right: bool = False):
     """Forward statistics over a packed batch ``[total, H, d]``.
 
     cu_q / cu_kv are the cumulative offsets (``actual_q`` / ``actual_kv``,
@@ -152,13 +187,13 @@ def forward_packed(q, k, v, cu_q, cu_kv, scale: float, causal: bool,
         qs, qe = cu_q[b], cu_q[b + 1]
         ks, ke = cu_kv[b], cu_kv[b + 1]
         hk = _kv_head(h, H, Hkv)
-        ob, mb, lb = forward_head(q[qs:qe, h], k[ks:ke, hk], v[ks:ke, hk], scale, causal)
+        ob, mb, lb = forward_head(q[qs:qe, h], k[ks:ke, hk], v[ks:ke, hk], scale, causal, window, bottom_right)
         o[qs:qe, h], m[qs:qe, h], l[qs:qe, h] = ob, mb, lb
     return o, m, l
 
 
 def backward_packed(q, k, v, o, do, m, l, cu_q, cu_kv, scale: float,
-                    causal: bool, heads_subset=None):
+                    causal: bool, heads_subset=None, window: int = 0, bottom_right: bool = False):
     """Backward over a packed batch from the given (O, m, l).
 
     Returns float64 dQ [total_q,H,d], dK and dV [total_kv,Hkv,d] and
@@ -183,7 +218,7 @@ def backward_packed(q, k, v, o, do, m, l, cu_q, cu_kv, scale: float,
         ks, ke = cu_kv[b], cu_kv[b + 1]
         hk = _kv_head(h, H, Hkv)
         r = backward_head(q[qs:qe, h], k[ks:ke, hk], v[ks:ke, hk], o[qs:qe, h],
-                          do[qs:qe, h], m[qs:qe, h], l[qs:qe, h], scale, causal)
+                          do[qs:qe, h], m[qs:qe, h], l[qs:qe, h], scale, causal, window, bottom_right)
         dq[qs:qe, h], D[qs:qe, h] = r[0], r[3]
         dk[ks:ke, hk] += r[1]
         dv[ks:ke, hk] += r[2]
