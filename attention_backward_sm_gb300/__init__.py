@@ -27,6 +27,18 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_DQ_ATOMIC = 0
 FA_DQ_DETERMINISTIC = 1
+FA_MASK_NONE = 0
+FA_MASK_CAUSAL = 1
+FA_MASK_CAUSAL_BOTTOM_RIGHT = 2
+
+
+def mask_kind(causal: bool, bottom_right: bool = False) -> int:
+    """fa_mask value for a causal flag and an alignment."""
+    if not causal:
+        if bottom_right:
+            raise ValueError("bottom_right needs causal")
+        return FA_MASK_NONE
+    return FA_MASK_CAUSAL_BOTTOM_RIGHT if bottom_right else FA_MASK_CAUSAL
 
 
 class FabwdError(RuntimeError):
@@ -98,6 +110,17 @@ def fa_fwd_stats_gqa(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_hos
                                   dim, int(bool(causal)), float(scale), _stream(stream)))
 
 
+def fa_fwd_stats_ex(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask: int, window: int,
+                    scale: float, stream=None):
+    """fa_fwd_stats_gqa with an fa_mask value and a sliding window (0 = none)."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv, heads_kv = int(k.shape[0]), int(k.shape[1])
+    _check(lib().fa_fwd_stats_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(m), _ptr(l), _ptr(cu_q_dev),
+                                 _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1, total_q, total_kv, heads, heads_kv,
+                                 dim, int(mask), int(window), float(scale), _stream(stream)))
+
+
 def fa_bwd_preprocess(o, do, D, dq_acc, stream=None):
     total_q, heads, dim = _shape(o)
     _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(D), _ptr(dq_acc), total_q, heads, dim,
@@ -138,6 +161,19 @@ def fa_bwd_gqa(q, k, v, do, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_h
                             _ptr(workspace), ws_bytes, _stream(stream)))
 
 
+def fa_bwd_ex(q, k, v, do, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask: int,
+              window: int, scale: float, dq_mode: int = FA_DQ_ATOMIC, workspace=None, stream=None):
+    """fa_bwd_gqa with an fa_mask value and a sliding window (0 = none)."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv, heads_kv = int(k.shape[0]), int(k.shape[1])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(m), _ptr(l), _ptr(D), _ptr(dq_acc),
+                           _ptr(dk), _ptr(dv), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1,
+                           total_q, total_kv, heads, heads_kv, dim, int(mask), int(window), float(scale),
+                           int(dq_mode), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
 def fa_bwd_dq_finalize(dq_acc, dq, scale: float, stream=None):
     total_q, heads, dim = _shape(dq)
     _check(lib().fa_bwd_dq_finalize(_ptr(dq_acc), _ptr(dq), total_q, heads, dim, float(scale), _stream(stream)))
@@ -159,13 +195,16 @@ def fa_check_device_status(stream=None):
     _check(lib().fa_check_device_status(_stream(stream)))
 
 
-def forward_stats(q, k, v, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float, stream=None):
-    """Allocates and returns (o, m, l) from fa_fwd_stats."""
+def forward_stats(q, k, v, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float, stream=None,
+                  window: int = 0, bottom_right: bool = False):
+    """Allocates and returns (o, m, l) from fa_fwd_stats_ex (k, v may have
+    fewer heads than q; window > 0 is a causal sliding window)."""
     total_q, heads, dim = _shape(q)
     o = torch.zeros_like(q)
     m = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
     l = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
-    fa_fwd_stats_gqa(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal, scale, stream)
+    fa_fwd_stats_ex(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask_kind(causal, bottom_right),
+                    window, scale, stream)
     return o, m, l
 
 
@@ -181,16 +220,19 @@ class Workspace:
 
 
 def backward(q, k, v, o, do, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
-             dq_mode: int = FA_DQ_ATOMIC, out=None, work: Workspace | None = None, stream=None):
-    """preprocess -> fa_bwd -> finalize on one stream; returns (dq, dk, dv).
-    k and v may have fewer heads than q (grouped-query attention)."""
+             dq_mode: int = FA_DQ_ATOMIC, out=None, work: Workspace | None = None, stream=None,
+             window: int = 0, bottom_right: bool = False):
+    """preprocess -> fa_bwd_ex -> finalize on one stream; returns (dq, dk, dv).
+    k and v may have fewer heads than q (grouped-query attention); the mask
+    is none, causal (top-left, or bottom-right) and optionally a causal
+    sliding window of `window` keys."""
     if work is None:
         work = Workspace(q, cu_q_host, cu_kv_host, causal, dq_mode)
     if out is None:
         out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     dq, dk, dv = out
     fa_bwd_preprocess(o, do, work.D, work.dq_acc, stream)
-    fa_bwd_gqa(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal,
-               scale, dq_mode, work.ws, stream)
+    fa_bwd_ex(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host,
+              mask_kind(causal, bottom_right), window, scale, dq_mode, work.ws, stream)
     fa_bwd_dq_finalize(work.dq_acc, dq, scale, stream)
     return dq, dk, dv

@@ -68,6 +68,22 @@ int check_shape(int batch, int total_q, int total_kv, int heads, int head_dim) {
   return FA_OK;
 }
 
+int check_mask(int mask, int window) {
+  if (mask != FA_MASK_NONE && mask != FA_MASK_CAUSAL && mask != FA_MASK_CAUSAL_BOTTOM_RIGHT)
+    return fail(FA_ERR_INVALID_ARG, "mask must be 0 (none), 1 (causal) or 2 (causal, bottom-right), got %d", mask);
+  if (window < 0) return fail(FA_ERR_INVALID_ARG, "window must be >= 0, got %d", window);
+  if (window > 0 && mask == FA_MASK_NONE)
+    return fail(FA_ERR_INVALID_ARG, "a sliding window needs a causal mask (it sees the keys (pos - window, pos])");
+  return FA_OK;
+}
+
+// A window at least as long as both sequences together excludes no key that
+// the causal mask admits; it is dropped so that device arithmetic on it
+// cannot overflow.
+int effective_window(int window, int max_q, int max_kv) {
+  return static_cast<long long>(window) >= static_cast<long long>(max_q) + max_kv ? 0 : window;
+}
+
 int check_groups(int heads, int heads_kv) {
   if (heads_kv < 1 || heads % heads_kv != 0)
     return fail(FA_ERR_INVALID_ARG, "query heads (%d) must be a positive multiple of key/value heads (%d)", heads,
@@ -136,14 +152,14 @@ extern "C" {
 
 const char* fa_last_error(void) { return g_err; }
 
-int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
-                     const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
-                     const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int heads_kv,
-                     int head_dim, int causal, float scale, fa_stream_t stream) {
+int fa_fwd_stats_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
+                    const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
+                    const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int heads_kv,
+                    int head_dim, int mask, int window, float scale, fa_stream_t stream) {
   int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
   if (rc) return rc;
   if ((rc = check_groups(heads, heads_kv))) return rc;
-  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  if ((rc = check_mask(mask, window))) return rc;
   if (!isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
   int max_q = 0, max_kv = 0;
   if ((rc = check_offsets(cu_q_host, batch, total_q, "cu_q", &max_q))) return rc;
@@ -163,19 +179,31 @@ int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf
   p.cu_kv = cu_kv_dev;
   p.heads = heads;
   p.heads_kv = heads_kv;
-  p.causal = causal;
+  p.causal = mask != FA_MASK_NONE;
+  p.bottom_right = mask == FA_MASK_CAUSAL_BOTTOM_RIGHT;
+  p.window = effective_window(window, max_q, max_kv);
   p.scale = scale;
   cudaError_t e = fa::launch_fwd_stats(p, head_dim, batch, (max_q + 63) / 64, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fwd_stats launch");
   return ok();
 }
 
+int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
+                     const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
+                     const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int heads_kv,
+                     int head_dim, int causal, float scale, fa_stream_t stream) {
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  return fa_fwd_stats_ex(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q, total_kv,
+                         heads, heads_kv, head_dim, causal, 0, scale, stream);
+}
+
 int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
                  const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
                  const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int head_dim, int causal,
                  float scale, fa_stream_t stream) {
-  return fa_fwd_stats_gqa(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q, total_kv,
-                          heads, heads, head_dim, causal, scale, stream);
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  return fa_fwd_stats_ex(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q, total_kv,
+                         heads, heads, head_dim, causal, 0, scale, stream);
 }
 
 int fa_bwd_preprocess(const fa_bf16* o, const fa_bf16* dout, float* D, float* dq_acc, int total_q, int heads,
@@ -218,15 +246,16 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   return ((n * 4 + 255) / 256) * 256;
 }
 
-int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
-               const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
-               const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
-               int total_kv, int heads, int heads_kv, int head_dim, int causal, float scale, int dq_mode,
-               void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
+              const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
+              const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
+              int total_kv, int heads, int heads_kv, int head_dim, int mask, int window, float scale, int dq_mode,
+              void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
   if (rc) return rc;
   if ((rc = check_groups(heads, heads_kv))) return rc;
-  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  if ((rc = check_mask(mask, window))) return rc;
+  const int causal = mask != FA_MASK_NONE;
   if (dq_mode != FA_DQ_ATOMIC && dq_mode != FA_DQ_DETERMINISTIC)
     return fail(FA_ERR_INVALID_ARG, "dq_mode must be 0 or 1, got %d", dq_mode);
   if (!isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
@@ -283,6 +312,8 @@ int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf
   p.heads = heads;
   p.heads_kv = heads_kv;
   p.causal = causal;
+  p.bottom_right = mask == FA_MASK_CAUSAL_BOTTOM_RIGHT;
+  p.window = effective_window(window, max_q, max_kv);
   p.dq_mode = dq_mode;
   p.max_q_blocks = (max_q + 127) / 128;
   p.kv_reverse = (dq_mode == FA_DQ_DETERMINISTIC && causal) ? 1 : 0;
@@ -298,14 +329,26 @@ int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf
   return ok();
 }
 
+int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
+               const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
+               const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
+               int total_kv, int heads, int heads_kv, int head_dim, int causal, float scale, int dq_mode,
+               void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  return fa_bwd_ex(q, k, v, dout, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch,
+                   total_q, total_kv, heads, heads_kv, head_dim, causal, 0, scale, dq_mode, workspace,
+                   workspace_bytes, stream);
+}
+
 int fa_bwd(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m, const float* l,
            const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
            const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads,
            int head_dim, int causal, float scale, int dq_mode, void* workspace, size_t workspace_bytes,
            fa_stream_t stream) {
-  return fa_bwd_gqa(q, k, v, dout, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch,
-                    total_q, total_kv, heads, heads, head_dim, causal, scale, dq_mode, workspace, workspace_bytes,
-                    stream);
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", causal);
+  return fa_bwd_ex(q, k, v, dout, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch,
+                   total_q, total_kv, heads, heads, head_dim, causal, 0, scale, dq_mode, workspace, workspace_bytes,
+                   stream);
 }
 
 int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads, int head_dim, float scale,

@@ -155,13 +155,15 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first, int lane) {
 // P = 2^(S*scale*log2e - lse2) (= exp(S*scale - m) / l), zeroes masked
 // entries when MASK, and stores P as bf16 into the first 32 of the 64
 // columns just read.  MASK is a template parameter so that full blocks run
-// a loop without any per-element mask work.
+// a loop without any per-element mask work.  Every mask (tails, causal
+// in either alignment, sliding window) leaves key row r a single run of
+// visible query columns of the tile: [c_lo, c_lo + span) (span <= 0: none).
 // lse4: the 64 per-column lse2 values in shared memory; pre: the first 32
 // of them, read earlier.  The second 32 are read while the first TMEM load
 // is in flight.
 template <bool MASK>
 __device__ __forceinline__ void softmax_p(uint32_t taddr, const float4* lse4, const float4 (&pre)[8], float sl2,
-                                          float (&P)[64], int r, int qc0, int kv_valid, int q_valid, bool diag) {
+                                          float (&P)[64], int qc0, int c_lo, int span) {
   float4 nxt[8];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
@@ -181,9 +183,7 @@ __device__ __forceinline__ void softmax_p(uint32_t taddr, const float4* lse4, co
         const int col = half * 32 + c4 * 4 + e;
         float pv = ex2_approx(fmaf(__uint_as_float(v[c4 * 4 + e]), sl2, -la[e]));
         if (MASK) {
-          const int qc = qc0 + col;
-          // top-left causal: query qc sees key r iff qc >= r inside the diagonal block
-          const bool vis = (r < kv_valid) && (qc < q_valid) && (!diag || qc >= r);
+          const bool vis = static_cast<unsigned>(qc0 + col - c_lo) < static_cast<unsigned>(span);
           pv = vis ? pv : 0.f;
         }
         P[col] = pv;
@@ -237,6 +237,13 @@ __device__ __forceinline__ void softmax_ds(uint32_t taddr, const float4* dvec4, 
   }
 }
 
+// Floor of a / b for b > 0 and any sign of a.
+__device__ __forceinline__ int floordiv(long long a, int b) {
+  long long q = a / b;
+  if ((a % b) != 0 && a < 0) --q;
+  return static_cast<int>(q);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
@@ -265,8 +272,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   }
   const int kv_valid = min(BM, s2 - kvb * BM);
   const int n_qb = (s1 + BN - 1) / BN;
-  const int qb0 = p.causal ? kvb : 0;               // top-left mask: query block >= key block
-  const int n_qit = max(0, n_qb - qb0);             // query blocks per query head
+  // Mask band: query i sees key j iff j <= i + off (causal) and
+  // j > i + off - W (window W > 0); off = s2 - s1 for the bottom-right
+  // alignment, else 0.  A tile (query block, key block) is visited iff the
+  // band meets it; this key block's visited query blocks are [qb0, qb_hi].
+  const int off = p.bottom_right ? s2 - s1 : 0;
+  const int W = p.window;
+  const int qb0 = p.causal ? max(0, floordiv(static_cast<long long>(kvb) * BM - off, BN)) : 0;
+  const int qb_hi = (p.causal && W > 0) ? min(n_qb - 1, floordiv(static_cast<long long>(kvb) * BM + BM - 2 - off + W, BN))
+                                        : n_qb - 1;
+  const int n_qit = max(0, qb_hi - qb0 + 1);        // query blocks per query head
   const int n_it = G * n_qit;                       // iterations of the sweep
   const int n_kvb = (s2 + BM - 1) / BM;
   const int nq_div = max(1, n_qit);                 // divisor that stays valid when there is no work
@@ -538,9 +553,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const int s = k & 1;
       const uint32_t ph = k & 1;
       const int qb = qb_of(k);
-      const int q_valid = min(BN, s1 - qb * BN);
-      const bool diag = p.causal && (qb == kvb);
-      const bool need_mask = diag || q_valid < BN || kv_valid < BM;
+      // visible query columns of key row r in this tile: [c_lo, c_lo + span)
+      int c_lo = 0, c_end = min(BN, s1 - qb * BN);
+      if (p.causal) {
+        const long long d0 = static_cast<long long>(kvb) * BM + r - off - static_cast<long long>(qb) * BN;
+        c_lo = static_cast<int>(max(0LL, min(d0, static_cast<long long>(BN))));
+        if (W > 0) c_end = static_cast<int>(max(0LL, min(static_cast<long long>(c_end), d0 + W)));
+      }
+      const int span = (r < kv_valid) ? max(0, c_end - c_lo) : 0;
+      const bool need_mask = __any_sync(0xffffffffu, c_lo > wg * 64 || c_lo + span < wg * 64 + 64);
       if (!mbar_wait(bar(B_Q_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
       // The 64 per-column statistics are read into registers before the
       // scores are waited for: shared-memory loads queue behind the MMAs'
@@ -556,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       float P[64];
       const uint32_t t_srow = tmem + lane_addr + COL_S + wg * 64;
       if (need_mask)
-        softmax_p<true>(t_srow, lse4, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
+        softmax_p<true>(t_srow, lse4, lsev, sl2, P, wg * 64, c_lo, span);
       else
-        softmax_p<false>(t_srow, lse4, lsev, sl2, P, r, wg * 64, kv_valid, q_valid, diag);
+        softmax_p<false>(t_srow, lse4, lsev, sl2, P, wg * 64, c_lo, span);
       tc_fence_before();
       mbar_arrive(bar(B_P_READY));
 
@@ -662,9 +683,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       __syncwarp();
       bool turn = true;
       if (lane == 0 && det) {
-        // partials that come before this one: key blocks 0..kvb-1 (ascending
-        // order), or key blocks kvb+1..min(qb, n_kvb-1) (descending order)
-        const int before = p.kv_reverse ? min(qb, n_kvb - 1) - kvb : kvb;
+        // partials that come before this one: those of the key blocks
+        // kb_lo..kvb-1 (ascending order) or kvb+1..kb_hi (descending order),
+        // [kb_lo, kb_hi] being the key blocks whose tiles with query block qb
+        // the mask band meets
+        const long long q0 = static_cast<long long>(qb) * BN;
+        const int kb_hi = p.causal ? min(n_kvb - 1, floordiv(q0 + BN - 1 + off, BM)) : n_kvb - 1;
+        const int kb_lo = (p.causal && W > 0) ? max(0, floordiv(q0 + off - W + 1, BM)) : 0;
+        const int before = p.kv_reverse ? kb_hi - kvb : kvb - kb_lo;
         turn = wait_counter(ticket, before, abort, status);
         fence_proxy_async_global();
       }

@@ -4,6 +4,9 @@
 // (section 3.1 step 2) defines P from exactly these m and l; section 5
 // names the online-softmax forward skeleton as their producer.
 //
+// Masks: none, causal aligned top-left or bottom-right, and the causal
+// sliding window (JAX dot_product_attention, sliding_window_length).
+//
 // One CTA computes a 64-row query block of one (sequence, query head; the
 // key/value head is shared by a group of query heads) with an
 // online softmax over 64-row key blocks, on the CUDA cores in fp32 (every
@@ -66,13 +69,20 @@ __global__ void __launch_bounds__(256) fwd_stats_kernel(const FwdParams p) {
     for (int c = 0; c < OC; ++c) acc[i][c] = 0.f;
   }
 
-  // Keys visible to this block: all of them, or (top-left causal) those
-  // with local index <= the block's last query index.
-  int kv_end = s2;
-  if (p.causal) kv_end = min(s2, qb * BQ + BQ);
-  const int nkb = (kv_end + BK - 1) / BK;
+  // Query i sees key j iff j <= i + off (causal; off = s2 - s1 for the
+  // bottom-right alignment, else 0) and j > i + off - W (window W > 0).
+  // Keys any row of this block sees: [kv_begin, kv_end).
+  const long long off = p.bottom_right ? static_cast<long long>(s2) - s1 : 0;
+  const int W = p.window;
+  long long kv_begin = 0, kv_end = s2;
+  if (p.causal) {
+    kv_end = min(kv_end, static_cast<long long>(qb) * BQ + BQ + off);
+    if (W > 0) kv_begin = max(0LL, static_cast<long long>(qb) * BQ + off - W + 1);
+  }
+  const int kb_first = static_cast<int>(kv_begin / BK);
+  const int kb_end = kv_end > kv_begin ? static_cast<int>((kv_end + BK - 1) / BK) : kb_first;
 
-  for (int kb = 0; kb < nkb; ++kb) {
+  for (int kb = kb_first; kb < kb_end; ++kb) {
     __syncthreads();
     for (int e = tid; e < BK * D; e += 256) {
       const int r = e / D, c = e % D;
@@ -109,12 +119,13 @@ __global__ void __launch_bounds__(256) fwd_stats_kernel(const FwdParams p) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int kj = kb * BK + cg * 4 + j;
-        const bool ok = kj < s2 && (!p.causal || kj <= qi);
+        const long long rel = static_cast<long long>(kj) - qi - off;   // j - (i + off)
+        const bool ok = kj < s2 && (!p.causal || (rel <= 0 && (W <= 0 || rel > -W)));
         x[j] = ok ? s[i][j] * p.scale : -INFINITY;
         mx = fmaxf(mx, x[j]);
       }
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      for (int sh = 8; sh > 0; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
       const float m_new = fmaxf(m_run[i], mx);
       // Rows that have seen no visible key yet keep m = -inf and P = 0.
       const float alpha = (m_new == -INFINITY) ? 1.f : expf(m_run[i] - m_new);
@@ -126,7 +137,7 @@ __global__ void __launch_bounds__(256) fwd_stats_kernel(const FwdParams p) {
         pT[(cg * 4 + j) * LD + rg * 4 + i] = pj;
       }
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
+      for (int sh = 8; sh > 0; sh >>= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, sh);
       l_run[i] = l_run[i] * alpha + rsum;
       m_run[i] = m_new;
 #pragma unroll

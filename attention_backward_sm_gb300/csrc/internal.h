@@ -28,7 +28,9 @@ struct BwdParams {
   int* tickets;        // deterministic mode: one counter per (batch, head, query block, 32-row quarter)
   int heads;           // query heads
   int heads_kv;        // key/value heads (heads is a multiple of it)
-  int causal;
+  int causal;          // 1: causal mask (top-left unless bottom_right)
+  int bottom_right;    // 1: causal diagonal aligned with the last key (offset s2 - s1 per sequence)
+  int window;          // > 0: sliding window, query i sees keys (i + off - window, i + off]
   int dq_mode;
   int max_q_blocks;    // query blocks of the longest query sequence
   int kv_reverse;      // 1: blockIdx.x counts key blocks from the last one down
@@ -55,7 +57,9 @@ struct FwdParams {
   const int32_t* cu_kv;
   int heads;           // query heads
   int heads_kv;        // key/value heads (heads is a multiple of it)
-  int causal;
+  int causal;          // as in BwdParams
+  int bottom_right;
+  int window;
   float scale;
 };
 cudaError_t launch_fwd_stats(const FwdParams& p, int head_dim, int batch, int max_q_blocks64, cudaStream_t s);

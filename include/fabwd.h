@@ -59,9 +59,21 @@ enum fa_status {
 
 enum fa_dq_mode {
     FA_DQ_ATOMIC = 0,         /* dQ partials added with fp32 atomics, in any order */
-    FA_DQ_DETERMINISTIC = 1   /* dQ partials added in ascending key-block order: bitwise reproducible;
+    FA_DQ_DETERMINISTIC = 1   /* dQ partials added in a fixed key-block order: bitwise reproducible;
                                  needs fa_bwd_workspace_size() bytes of workspace (one int32 counter
                                  per batch x head x 128-row query block x 32-row quarter) */
+};
+
+/* Masks of the _ex entry points (local indices i of the query, j of the key
+ * within one sequence of s1 queries and s2 keys).  JAX
+ * fused_attention_stablehlo.py, MaskType and the sliding_window_length
+ * argument of dot_product_attention. */
+enum fa_mask {
+    FA_MASK_NONE = 0,                  /* every key visible */
+    FA_MASK_CAUSAL = 1,                /* top-left: j <= i (MaskType.CAUSAL) */
+    FA_MASK_CAUSAL_BOTTOM_RIGHT = 2    /* diagonal through the last key: j <= i + s2 - s1
+                                          (the pages define no alignment for s1 != s2;
+                                          this is the other usual one) */
 };
 
 /* Forward statistics used to build consistent backward inputs (support
@@ -80,7 +92,8 @@ int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
 /* fa_fwd_stats for grouped-query attention: k and v have heads_kv heads
  * ([total_kv, heads_kv, d]); query head h uses key/value head
  * h / (heads / heads_kv) (consecutive groups; the JAX cuDNN wrapper's
- * q_N != kv_N case, page 3 `_dot_product_attention_bwd_cuda_lowering`).
+ * q_N != kv_N case of JAX fused_attention_stablehlo.py,
+ * `_dot_product_attention_bwd_cuda_lowering`).
  * heads must be a positive multiple of heads_kv.  fa_fwd_stats is this
  * call with heads_kv = heads. */
 int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
@@ -89,6 +102,19 @@ int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
                      const int32_t* cu_q_host, const int32_t* cu_kv_host,
                      int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
                      int causal, float scale, fa_stream_t stream);
+
+/* fa_fwd_stats_gqa with a mask and a sliding window: mask is an fa_mask;
+ * window = W > 0 restricts a causal mask to the left window (pos - W, pos]
+ * with pos = i (top-left) or i + s2 - s1 (bottom-right), i.e. query i sees
+ * keys j with pos - W < j <= pos (JAX dot_product_attention,
+ * sliding_window_length); window = 0 means no window, and a window needs
+ * a causal mask.  Rows that see no key get O = 0, m = -inf, l = 0. */
+int fa_fwd_stats_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
+                    fa_bf16* o, float* m, float* l,
+                    const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+                    const int32_t* cu_q_host, const int32_t* cu_kv_host,
+                    int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
+                    int mask, int window, float scale, fa_stream_t stream);
 
 /* Backward preprocess (section 3.1 step 4; section 4.2 row "D"):
  * D[r, h] = sum_k float(O[r,h,k]) * float(dO[r,h,k]) for every row
@@ -141,6 +167,21 @@ int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf
                int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
                int causal, float scale, int dq_mode,
                void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* fa_bwd_gqa with a mask and a sliding window (as in fa_fwd_stats_ex).
+ * A CTA visits only the query blocks whose tiles the band of visible
+ * (query, key) pairs meets; gradients of keys no query sees are exact
+ * zeros.  fa_bwd and fa_bwd_gqa are this call with mask = causal and
+ * window = 0.  In FA_DQ_DETERMINISTIC mode the key-block order of the dQ
+ * additions is fixed for a given mask, so runs are bitwise reproducible. */
+int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout,
+              const float* m, const float* l, const float* D,
+              float* dq_acc, fa_bf16* dk, fa_bf16* dv,
+              const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+              const int32_t* cu_q_host, const int32_t* cu_kv_host,
+              int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
+              int mask, int window, float scale, int dq_mode,
+              void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* dQ write-back (section 3, V2 applies scale to dq; section 4.2 row dQ:
  * fp32 accumulate, then bf16): dq[e] = bf16_rne(scale * dq_acc[e]) for all

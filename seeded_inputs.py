@@ -63,6 +63,8 @@ class Case:
     pad_kv: int = 0     # NaN rows appended after the last key row
     scale: float | None = None
     heads_kv: int | None = None   # key/value heads (grouped-query attention); None = heads
+    window: int = 0               # causal sliding-window length (0 = none)
+    bottom_right: bool = False    # causal diagonal aligned with the last key
 
     @property
     def batch(self) -> int:

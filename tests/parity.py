@@ -20,9 +20,8 @@ MAX_ABS = 3e-2
 
 def structural_zero_rows(case: si.Case):
     """Rows whose gradients are exactly zero by construction, independent of
-    rounding: padding rows, queries of sequences without keys, and keys that
-    no query sees (sequences without queries; keys j >= s1 under the
-    top-left causal mask)."""
+    rounding: padding rows, queries that see no key and keys that no query
+    sees (the oracle's visibility rule for the case's mask)."""
     zq = np.zeros(case.total_q, dtype=bool)
     zk = np.zeros(case.total_kv, dtype=bool)
     zq[int(case.cu_q[-1]):] = True
@@ -30,12 +29,9 @@ def structural_zero_rows(case: si.Case):
     for b in range(case.batch):
         q0, q1 = int(case.cu_q[b]), int(case.cu_q[b + 1])
         k0, k1 = int(case.cu_kv[b]), int(case.cu_kv[b + 1])
-        if k1 == k0:
-            zq[q0:q1] = True
-        if q1 == q0:
-            zk[k0:k1] = True
-        elif case.causal:
-            zk[k0 + min(q1 - q0, k1 - k0):k1] = True
+        vis = oracle.visible(q1 - q0, k1 - k0, case.causal, case.window, case.bottom_right)
+        zq[q0:q1] = ~vis.any(axis=1)
+        zk[k0:k1] = ~vis.any(axis=0)
     return zq, zk
 
 
@@ -78,8 +74,9 @@ class Prepared:
         self.cu_q = torch.from_numpy(case.cu_q).to(dev)
         self.cu_kv = torch.from_numpy(case.cu_kv).to(dev)
         self.q, self.k, self.v, self.do = (t.to(dev) for t in (q, k, v, do))
+        self.mask_kw = dict(window=case.window, bottom_right=case.bottom_right)
         o64, m64, l64 = oracle.forward_packed(q, k, v, case.cu_q, case.cu_kv, self.scale, case.causal,
-                                              heads_subset=heads_subset)
+                                              heads_subset=heads_subset, **self.mask_kw)
         o = torch.from_numpy(o64).to(torch.bfloat16)
         m = torch.from_numpy(m64).to(torch.float32)
         l = torch.from_numpy(l64).to(torch.float32)
@@ -87,7 +84,7 @@ class Prepared:
             self.o, self.m, self.l = o.to(dev), m.to(dev), l.to(dev)
         else:
             self.o, self.m, self.l = fab.forward_stats(self.q, self.k, self.v, self.cu_q, self.cu_kv, case.cu_q,
-                                                       case.cu_kv, case.causal, self.scale)
+                                                       case.cu_kv, case.causal, self.scale, **self.mask_kw)
             for b, h in heads_subset:
                 rows = slice(int(case.cu_q[b]), int(case.cu_q[b + 1]))
                 self.o[rows, h] = o[rows, h].to(dev)
@@ -101,12 +98,12 @@ class Prepared:
         q, k, v, do = self.cpu
         return oracle.backward_packed(q, k, v, self.o_cpu, do, self.m_cpu, self.l_cpu, self.case.cu_q,
                                       self.case.cu_kv, self.scale, self.case.causal,
-                                      heads_subset=self.heads_subset)
+                                      heads_subset=self.heads_subset, **self.mask_kw)
 
     def run(self, dq_mode=0):
         import attention_backward_sm_gb300 as fab
         out = fab.backward(self.q, self.k, self.v, self.o, self.do, self.m, self.l, self.cu_q, self.cu_kv,
-                           self.case.cu_q, self.case.cu_kv, self.case.causal, self.scale, dq_mode)
+                           self.case.cu_q, self.case.cu_kv, self.case.causal, self.scale, dq_mode, **self.mask_kw)
         torch.cuda.synchronize()
         fab.fa_check_device_status()
         return out
