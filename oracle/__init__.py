@@ -13,4 +13,7 @@ from .attention import (  # noqa: F401
     rowsum_o_do,
     masked_scores,
     visible,
+    lse_from_stats,
+    backward_head_lse,
+    backward_packed_lse,
 )

@@ -192,6 +192,61 @@ def forward_packed(q, k, v, cu_q, cu_kv, scale: float, causal: bool,
     return o, m, l
 
 
+def lse_from_stats(m, l) -> np.ndarray:
+    """The single softmax statistic lse_i = log(sum_j exp(X_ij)) = m_i + log(l_i)
+    (natural log; -inf for rows that see no key).  JAX's cuDNN wrapper keeps
+    one float32 ``softmax_stat`` per query row between forward and backward;
+    this is the reading of what it holds."""
+    m, l = _f64(m), _f64(l)
+    out = np.full(m.shape, -np.inf)
+    rows = l > 0
+    out[rows] = m[rows] + np.log(l[rows])
+    return out
+
+
+def backward_head_lse(q, k, v, o, do, lse, scale: float, causal: bool, window: int = 0,
+                      bottom_right: bool = False):
+    """backward_head with P = exp(X - lse) from the single statistic lse
+    instead of exp(X - m) / l; the other steps are the same."""
+    q, k, v, o, do = (_f64(t) for t in (q, k, v, o, do))
+    lse = _f64(lse)
+    s1, s2 = q.shape[0], k.shape[0]
+    D = rowsum_o_do(o, do)
+    if s1 == 0 or s2 == 0:
+        return (np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), D)
+    x = masked_scores(q, k, scale, causal, window, bottom_right)
+    rows = np.isfinite(lse)
+    p = np.zeros_like(x)
+    p[rows] = np.exp(x[rows] - lse[rows][:, None])
+    dp = do @ v.T
+    ds = p * (dp - D[:, None])
+    return scale * (ds @ k), scale * (ds.T @ q), p.T @ do, D
+
+
+def backward_packed_lse(q, k, v, o, do, lse, cu_q, cu_kv, scale: float, causal: bool, heads_subset=None,
+                        window: int = 0, bottom_right: bool = False):
+    """backward_packed from lse [total_q, H] instead of (m, l)."""
+    q, k, v, o, do = (_f64(t) for t in (q, k, v, o, do))
+    lse = _f64(lse)
+    cu_q = np.asarray(cu_q, dtype=np.int64)
+    cu_kv = np.asarray(cu_kv, dtype=np.int64)
+    H, Hkv = q.shape[1], k.shape[1]
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    D = np.zeros(q.shape[:2])
+    units = heads_subset if heads_subset is not None else [
+        (b, h) for b in range(len(cu_q) - 1) for h in range(H)]
+    for b, h in units:
+        qs, qe = cu_q[b], cu_q[b + 1]
+        ks, ke = cu_kv[b], cu_kv[b + 1]
+        hk = _kv_head(h, H, Hkv)
+        r = backward_head_lse(q[qs:qe, h], k[ks:ke, hk], v[ks:ke, hk], o[qs:qe, h], do[qs:qe, h],
+                              lse[qs:qe, h], scale, causal, window, bottom_right)
+        dq[qs:qe, h], D[qs:qe, h] = r[0], r[3]
+        dk[ks:ke, hk] += r[1]
+        dv[ks:ke, hk] += r[2]
+    return dq, dk, dv, D
+
+
 def backward_packed(q, k, v, o, do, m, l, cu_q, cu_kv, scale: float,
                     causal: bool, heads_subset=None, window: int = 0, bottom_right: bool = False):
     """Backward over a packed batch from the given (O, m, l).
