@@ -121,6 +121,17 @@ def fa_fwd_stats_ex(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host
                                  dim, int(mask), int(window), float(scale), _stream(stream)))
 
 
+def fa_fwd_lse(q, k, v, o, lse, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask: int, window: int, scale: float,
+               stream=None):
+    """fa_fwd_stats_ex writing lse = m + ln(l) per row instead of (m, l)."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv, heads_kv = int(k.shape[0]), int(k.shape[1])
+    _check(lib().fa_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq),
+                            _hp(ck), len(cq) - 1, total_q, total_kv, heads, heads_kv, dim, int(mask), int(window),
+                            float(scale), _stream(stream)))
+
+
 def fa_bwd_preprocess(o, do, D, dq_acc, stream=None):
     total_q, heads, dim = _shape(o)
     _check(lib().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(D), _ptr(dq_acc), total_q, heads, dim,
@@ -172,6 +183,19 @@ def fa_bwd_ex(q, k, v, do, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_ho
                            _ptr(dk), _ptr(dv), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1,
                            total_q, total_kv, heads, heads_kv, dim, int(mask), int(window), float(scale),
                            int(dq_mode), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fa_bwd_lse(q, k, v, do, lse, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask: int,
+               window: int, scale: float, dq_mode: int = FA_DQ_ATOMIC, workspace=None, stream=None):
+    """fa_bwd_ex from the single statistic lse instead of (m, l)."""
+    cq, ck = _host_offsets(cu_q_host), _host_offsets(cu_kv_host)
+    total_q, heads, dim = _shape(q)
+    total_kv, heads_kv = int(k.shape[0]), int(k.shape[1])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(D), _ptr(dq_acc), _ptr(dk),
+                            _ptr(dv), _ptr(cu_q_dev), _ptr(cu_kv_dev), _hp(cq), _hp(ck), len(cq) - 1, total_q,
+                            total_kv, heads, heads_kv, dim, int(mask), int(window), float(scale), int(dq_mode),
+                            _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def fa_bwd_dq_finalize(dq_acc, dq, scale: float, stream=None):
@@ -234,5 +258,32 @@ def backward(q, k, v, o, do, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, c
     fa_bwd_preprocess(o, do, work.D, work.dq_acc, stream)
     fa_bwd_ex(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host,
               mask_kind(causal, bottom_right), window, scale, dq_mode, work.ws, stream)
+    fa_bwd_dq_finalize(work.dq_acc, dq, scale, stream)
+    return dq, dk, dv
+
+
+def forward_lse(q, k, v, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float, stream=None,
+                window: int = 0, bottom_right: bool = False):
+    """Allocates and returns (o, lse) from fa_fwd_lse."""
+    total_q, heads, dim = _shape(q)
+    o = torch.zeros_like(q)
+    lse = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
+    fa_fwd_lse(q, k, v, o, lse, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask_kind(causal, bottom_right), window,
+               scale, stream)
+    return o, lse
+
+
+def backward_lse(q, k, v, o, do, lse, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
+                 dq_mode: int = FA_DQ_ATOMIC, out=None, work: Workspace | None = None, stream=None,
+                 window: int = 0, bottom_right: bool = False):
+    """backward() from the single statistic lse = m + ln(l)."""
+    if work is None:
+        work = Workspace(q, cu_q_host, cu_kv_host, causal, dq_mode)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    fa_bwd_preprocess(o, do, work.D, work.dq_acc, stream)
+    fa_bwd_lse(q, k, v, do, lse, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host,
+               mask_kind(causal, bottom_right), window, scale, dq_mode, work.ws, stream)
     fa_bwd_dq_finalize(work.dq_acc, dq, scale, stream)
     return dq, dk, dv

@@ -20,6 +20,7 @@ SIGNATURES = {
     "fa_fwd_stats": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p]),
     "fa_fwd_stats_gqa": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p]),
     "fa_fwd_stats_ex": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p]),
+    "fa_fwd_lse": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p]),
     "fa_bwd_preprocess": (_i, [_p, _p, _p, _p, _i, _i, _i, _p]),
     "fa_bwd_workspace_size": (_sz, [_p, _p, _i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
@@ -28,6 +29,8 @@ SIGNATURES = {
                         _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]),
     "fa_bwd_ex": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                        _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]),
+    "fa_bwd_lse": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                        _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p]),
     "fa_bwd_dq_finalize": (_i, [_p, _p, _i, _i, _i, _f, _p]),
     "fa_bwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                             _i, _i, _i, _i, _i, _i, _f, _p]),

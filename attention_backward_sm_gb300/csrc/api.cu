@@ -152,10 +152,14 @@ extern "C" {
 
 const char* fa_last_error(void) { return g_err; }
 
-int fa_fwd_stats_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
-                    const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
-                    const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int heads_kv,
-                    int head_dim, int mask, int window, float scale, fa_stream_t stream) {
+namespace {
+
+// Shared body of the forward-statistics entry points; stats_lse selects
+// lse = m + ln(l) written into m (l unused) instead of the pair (m, l).
+int fwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
+             const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host,
+             int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim, int mask, int window,
+             int stats_lse, float scale, fa_stream_t stream) {
   int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
   if (rc) return rc;
   if ((rc = check_groups(heads, heads_kv))) return rc;
@@ -165,7 +169,7 @@ int fa_fwd_stats_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf1
   if ((rc = check_offsets(cu_q_host, batch, total_q, "cu_q", &max_q))) return rc;
   if ((rc = check_offsets(cu_kv_host, batch, total_kv, "cu_kv", &max_kv))) return rc;
   if (batch == 0 || max_q == 0) return ok();
-  if (!q || !k || !v || !o || !m || !l || !cu_q_dev || !cu_kv_dev)
+  if (!q || !k || !v || !o || !m || (!stats_lse && !l) || !cu_q_dev || !cu_kv_dev)
     return fail(FA_ERR_INVALID_ARG, "a device pointer is NULL");
   if ((rc = check_device())) return rc;
   fa::FwdParams p{};
@@ -182,10 +186,29 @@ int fa_fwd_stats_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf1
   p.causal = mask != FA_MASK_NONE;
   p.bottom_right = mask == FA_MASK_CAUSAL_BOTTOM_RIGHT;
   p.window = effective_window(window, max_q, max_kv);
+  p.stats_lse = stats_lse;
   p.scale = scale;
   cudaError_t e = fa::launch_fwd_stats(p, head_dim, batch, (max_q + 63) / 64, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fwd_stats launch");
   return ok();
+}
+
+}  // namespace
+
+int fa_fwd_stats_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
+                    const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
+                    const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int heads_kv,
+                    int head_dim, int mask, int window, float scale, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q, total_kv, heads,
+                  heads_kv, head_dim, mask, window, 0, scale, stream);
+}
+
+int fa_fwd_lse(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* lse,
+               const int32_t* cu_q_dev, const int32_t* cu_kv_dev, const int32_t* cu_q_host,
+               const int32_t* cu_kv_host, int batch, int total_q, int total_kv, int heads, int heads_kv,
+               int head_dim, int mask, int window, float scale, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, nullptr, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q, total_kv,
+                  heads, heads_kv, head_dim, mask, window, 1, scale, stream);
 }
 
 int fa_fwd_stats_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, float* m, float* l,
@@ -246,11 +269,15 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   return ((n * 4 + 255) / 256) * 256;
 }
 
-int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
-              const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
-              const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
-              int total_kv, int heads, int heads_kv, int head_dim, int mask, int window, float scale, int dq_mode,
-              void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+namespace {
+
+// Shared body of the backward entry points; stats_lse: m holds lse and l is
+// unused.
+int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
+             const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
+             const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
+             int total_kv, int heads, int heads_kv, int head_dim, int mask, int window, int stats_lse, float scale,
+             int dq_mode, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
   if (rc) return rc;
   if ((rc = check_groups(heads, heads_kv))) return rc;
@@ -267,7 +294,7 @@ int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf1
   if (!has_work && total_kv == kv_used) return ok();
   if ((total_kv > 0 && (!dk || !dv)) ||
       (has_work && (!k || !v || !cu_q_dev || !cu_kv_dev)) ||
-      (has_work && max_q > 0 && (!q || !dout || !m || !l || !D || !dq_acc)))
+      (has_work && max_q > 0 && (!q || !dout || !m || (!stats_lse && !l) || !D || !dq_acc)))
     return fail(FA_ERR_INVALID_ARG, "a device pointer is NULL");
   const void* al[] = {q, k, v, dout, dq_acc, dk, dv};
   for (const void* ptr : al)
@@ -314,6 +341,7 @@ int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf1
   p.causal = causal;
   p.bottom_right = mask == FA_MASK_CAUSAL_BOTTOM_RIGHT;
   p.window = effective_window(window, max_q, max_kv);
+  p.stats_lse = stats_lse;
   p.dq_mode = dq_mode;
   p.max_q_blocks = (max_q + 127) / 128;
   p.kv_reverse = (dq_mode == FA_DQ_DETERMINISTIC && causal) ? 1 : 0;
@@ -327,6 +355,28 @@ int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf1
   cudaError_t e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, s);
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
   return ok();
+}
+
+}  // namespace
+
+int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
+              const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
+              const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
+              int total_kv, int heads, int heads_kv, int head_dim, int mask, int window, float scale, int dq_mode,
+              void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_impl(q, k, v, dout, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q,
+                  total_kv, heads, heads_kv, head_dim, mask, window, 0, scale, dq_mode, workspace, workspace_bytes,
+                  stream);
+}
+
+int fa_bwd_lse(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* lse,
+               const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
+               const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
+               int total_kv, int heads, int heads_kv, int head_dim, int mask, int window, float scale, int dq_mode,
+               void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_impl(q, k, v, dout, lse, nullptr, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch,
+                  total_q, total_kv, heads, heads_kv, head_dim, mask, window, 1, scale, dq_mode, workspace,
+                  workspace_bytes, stream);
 }
 
 int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,

@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           if (k < n_it && r < q_valid) {
             const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
             a[j] = __ldg(p.m + idx);
-            b[j] = __ldg(p.l + idx);
+            if (!p.stats_lse) b[j] = __ldg(p.l + idx);
             c[j] = __ldg(p.D + idx);
           }
         }
@@ -406,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         par_q = (k >> 1) & 1;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          st_lse[s * 128 + lane + 32 * j] = rm[j] * 1.4426950408889634f + __log2f(rl[j]);
+          // log2 of the softmax denominator, exp(x - m) / l = 2^(x*log2e - lse2)
+          st_lse[s * 128 + lane + 32 * j] = rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j]));
           st_D[s * 128 + lane + 32 * j] = rd[j];
         }
         if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;

@@ -174,8 +174,12 @@ __global__ void __launch_bounds__(256) fwd_stats_kernel(const FwdParams p) {
 #pragma unroll
     for (int c = 0; c < OC; ++c) p.o[row * rs + h * D + cg * OC + c] = f2bf(acc[i][c] * inv);
     if (cg == 0) {
-      p.m[row * H + h] = m_run[i];
-      p.l[row * H + h] = l_run[i];
+      if (p.stats_lse) {
+        p.m[row * H + h] = (l_run[i] > 0.f) ? m_run[i] + logf(l_run[i]) : -INFINITY;
+      } else {
+        p.m[row * H + h] = m_run[i];
+        p.l[row * H + h] = l_run[i];
+      }
     }
   }
 }

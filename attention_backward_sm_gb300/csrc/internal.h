@@ -31,6 +31,7 @@ struct BwdParams {
   int causal;          // 1: causal mask (top-left unless bottom_right)
   int bottom_right;    // 1: causal diagonal aligned with the last key (offset s2 - s1 per sequence)
   int window;          // > 0: sliding window, query i sees keys (i + off - window, i + off]
+  int stats_lse;       // 1: m holds lse = m + ln(l) per row and l is unused
   int dq_mode;
   int max_q_blocks;    // query blocks of the longest query sequence
   int kv_reverse;      // 1: blockIdx.x counts key blocks from the last one down
@@ -60,6 +61,7 @@ struct FwdParams {
   int causal;          // as in BwdParams
   int bottom_right;
   int window;
+  int stats_lse;       // 1: write lse = m + ln(l) into m and leave l untouched
   float scale;
 };
 cudaError_t launch_fwd_stats(const FwdParams& p, int head_dim, int batch, int max_q_blocks64, cudaStream_t s);

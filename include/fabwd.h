@@ -116,6 +116,18 @@ int fa_fwd_stats_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
                     int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
                     int mask, int window, float scale, fa_stream_t stream);
 
+/* fa_fwd_stats_ex writing the single softmax statistic per row instead of
+ * (m, l): lse[r, h] = m + ln(l) (natural log; -inf for rows that see no
+ * key).  JAX fused_attention_stablehlo.py keeps one float32 softmax_stat of
+ * shape (B, N, T) between its forward and backward calls; lse is the
+ * reading of what it holds.  lse: [total_q, H] float32. */
+int fa_fwd_lse(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
+               fa_bf16* o, float* lse,
+               const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+               const int32_t* cu_q_host, const int32_t* cu_kv_host,
+               int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
+               int mask, int window, float scale, fa_stream_t stream);
+
 /* Backward preprocess (section 3.1 step 4; section 4.2 row "D"):
  * D[r, h] = sum_k float(O[r,h,k]) * float(dO[r,h,k]) for every row
  * r < total_q, and dq_acc[r, h, :] = 0 (float32 accumulator of
@@ -182,6 +194,18 @@ int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf1
               int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
               int mask, int window, float scale, int dq_mode,
               void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* fa_bwd_ex consuming the single statistic lse = m + ln(l) (as written by
+ * fa_fwd_lse) instead of (m, l): P = exp(scale * S - lse).  Everything else,
+ * including the workspace, is as in fa_bwd_ex. */
+int fa_bwd_lse(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout,
+               const float* lse, const float* D,
+               float* dq_acc, fa_bf16* dk, fa_bf16* dv,
+               const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
+               const int32_t* cu_q_host, const int32_t* cu_kv_host,
+               int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
+               int mask, int window, float scale, int dq_mode,
+               void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* dQ write-back (section 3, V2 applies scale to dq; section 4.2 row dQ:
  * fp32 accumulate, then bf16): dq[e] = bf16_rne(scale * dq_acc[e]) for all
