@@ -10,6 +10,11 @@ come from the library's forward-statistics kernel before timing.
   python bench.py [--gpus N --steps K --warmup W] [--workload cfg3nc|cfg2|...]
   python bench.py --impl reference     # the fp64 CPU oracle on the same workload
 
+Variant workloads (--workload gqa|swa|br) exercise grouped-query attention,
+the causal sliding window and the bottom-right causal alignment; their FLOPs
+count 10*d per visible (query, key) pair.  --stats lse feeds the backward
+the single statistic lse = m + ln l instead of (m, l).
+
 Under torchrun every rank runs its own copy of the workload (the path
 shards over independent (sequence, head) units with no collective: weak
 scaling); rank 0 prints one JSON line with the max time over ranks.
@@ -136,8 +141,38 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+WORKLOADS = {**si.CONFIGS, **si.VARIANTS}
+
+
 def make_case(name: str) -> si.Case:
-    return si.CONFIGS[name]()
+    return WORKLOADS[name]()
+
+
+def visible_pairs(s1: int, s2: int, causal: bool, window: int = 0, bottom_right: bool = False,
+                  rows: int | None = None) -> int:
+    """Number of (query, key) pairs the mask admits among the first `rows`
+    queries: query i sees keys max(0, i+off-W+1) .. min(s2-1, i+off)
+    (causal; off = s2 - s1 bottom-right, else 0; W = window > 0)."""
+    n = s1 if rows is None else min(rows, s1)
+    if not causal:
+        return n * s2
+    i = np.arange(n, dtype=np.int64)
+    off = s2 - s1 if bottom_right else 0
+    hi = np.minimum(s2 - 1, i + off)
+    lo = np.maximum(0, i + off - window + 1) if window > 0 else np.zeros_like(i)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
+def useful_flops(case: si.Case) -> float:
+    """FLOPs of one backward: 10*s1*s2*d per (sequence, query head), halved
+    under the plain causal mask (the counting rule of the target metric);
+    for a sliding window or the bottom-right alignment, 10*d per visible
+    (query, key) pair, the same rule counted exactly."""
+    if case.window == 0 and not case.bottom_right:
+        return case.flops()
+    pairs = sum(visible_pairs(a, b, case.causal, case.window, case.bottom_right)
+                for a, b in zip(case.q_lens, case.kv_lens))
+    return 10.0 * pairs * case.head_dim * case.heads
 
 
 _TENSORS = {}
@@ -151,11 +186,20 @@ def case_tensors(case: si.Case):
 
 
 def workload_desc(case: si.Case) -> str:
+    mask = "non-causal"
+    if case.causal:
+        mask = "causal bottom-right" if case.bottom_right else "causal"
+        if case.window:
+            mask += f" window={case.window}"
+    heads = f"H={case.heads}" + (f" Hkv={case.kv_heads}" if case.kv_heads != case.heads else "")
     if len(set(case.q_lens)) == 1 and len(set(case.kv_lens)) == 1:
-        return (f"B={case.batch} H={case.heads} s1={case.q_lens[0]} s2={case.kv_lens[0]} d={case.head_dim} "
-                f"{'causal' if case.causal else 'non-causal'}")
-    return (f"varlen B={case.batch} H={case.heads} d={case.head_dim} q_lens={case.q_lens} "
-            f"kv_lens={case.kv_lens} {'causal' if case.causal else 'non-causal'}")
+        return (f"B={case.batch} {heads} s1={case.q_lens[0]} s2={case.kv_lens[0]} d={case.head_dim} {mask}")
+    return (f"varlen B={case.batch} {heads} d={case.head_dim} q_lens={case.q_lens} "
+            f"kv_lens={case.kv_lens} {mask}")
+
+
+def mask_kw(case: si.Case) -> dict:
+    return dict(window=case.window, bottom_right=case.bottom_right)
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -167,16 +211,20 @@ def oracle_sample(case: si.Case, budget_s: float, max_units: int | None = None):
     q, k, v, do = case_tensors(case)
     flops, secs, units = 0.0, 0.0, 0
     order = [(b, h) for b in range(case.batch) for h in range(case.heads)]
+    G = case.heads // case.kv_heads
     for b, h in order:
         qs, qe = int(case.cu_q[b]), int(case.cu_q[b + 1])
         ks, ke = int(case.cu_kv[b]), int(case.cu_kv[b + 1])
-        qq, kk, vv, dd = q[qs:qe, h], k[ks:ke, h], v[ks:ke, h], do[qs:qe, h]
-        o, m, l = oracle.forward_head(qq, kk, vv, case.softmax_scale, case.causal)   # inputs, untimed
+        qq, kk, vv, dd = q[qs:qe, h], k[ks:ke, h // G], v[ks:ke, h // G], do[qs:qe, h]
+        o, m, l = oracle.forward_head(qq, kk, vv, case.softmax_scale, case.causal, **mask_kw(case))   # untimed
         t0 = time.perf_counter()
-        oracle.backward_head(qq, kk, vv, o, dd, m, l, case.softmax_scale, case.causal)
+        oracle.backward_head(qq, kk, vv, o, dd, m, l, case.softmax_scale, case.causal, **mask_kw(case))
         secs += time.perf_counter() - t0
-        f = 10.0 * (qe - qs) * (ke - ks) * case.head_dim
-        flops += f / 2 if case.causal else f
+        if case.window == 0 and not case.bottom_right:
+            f = 10.0 * (qe - qs) * (ke - ks) * case.head_dim
+            flops += f / 2 if case.causal else f
+        else:
+            flops += 10.0 * case.head_dim * visible_pairs(qe - qs, ke - ks, True, case.window, case.bottom_right)
         units += 1
         if secs >= budget_s or (max_units and units >= max_units):
             break
@@ -198,17 +246,19 @@ def oracle_rows(case: si.Case, rows: int, b: int = 0, h: int = 0):
     q, k, v, do = case_tensors(case)
     qs = int(case.cu_q[b])
     ks, ke = int(case.cu_kv[b]), int(case.cu_kv[b + 1])
-    rows = max(1, min(rows, int(case.cu_q[b + 1]) - qs))
-    qq, kk, vv, dd = q[qs:qs + rows, h], k[ks:ke, h], v[ks:ke, h], do[qs:qs + rows, h]
-    o, m, l = oracle.forward_head(qq, kk, vv, case.softmax_scale, case.causal)   # inputs, untimed
+    s1, s2 = int(case.cu_q[b + 1]) - qs, ke - ks
+    rows = max(1, min(rows, s1))
+    hk = h // (case.heads // case.kv_heads)
+    if case.bottom_right:
+        # keys past what the first `rows` queries can see are dropped; the
+        # kept s2' = s2 - s1 + rows keys give the same bottom-right offset
+        ke = ks + max(0, min(s2, s2 - s1 + rows))
+    qq, kk, vv, dd = q[qs:qs + rows, h], k[ks:ke, hk], v[ks:ke, hk], do[qs:qs + rows, h]
+    o, m, l = oracle.forward_head(qq, kk, vv, case.softmax_scale, case.causal, **mask_kw(case))   # untimed
     t0 = time.perf_counter()
-    oracle.backward_head(qq, kk, vv, o, dd, m, l, case.softmax_scale, case.causal)
+    oracle.backward_head(qq, kk, vv, o, dd, m, l, case.softmax_scale, case.causal, **mask_kw(case))
     secs = time.perf_counter() - t0
-    s2 = ke - ks
-    if case.causal:
-        pairs = sum(min(i + 1, s2) for i in range(rows))
-    else:
-        pairs = rows * s2
+    pairs = visible_pairs(s1, s2, case.causal, case.window, case.bottom_right, rows)
     return 10.0 * pairs * case.head_dim, secs
 
 
@@ -272,20 +322,31 @@ def run_gpu(args):
     cu_q = torch.from_numpy(case.cu_q).to(dev)
     cu_kv = torch.from_numpy(case.cu_kv).to(dev)
     scale = case.softmax_scale
-    o, m, l = fab.forward_stats(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale)
+    mask = fab.mask_kind(case.causal, case.bottom_right)
+    lse_stats = args.stats == "lse"
+    if lse_stats:
+        o, lse = fab.forward_lse(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, **mask_kw(case))
+        stats = (lse,)
+    else:
+        o, m, l = fab.forward_stats(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, **mask_kw(case))
+        stats = (m, l)
     work = fab.Workspace(q, case.cu_q, case.cu_kv, case.causal, args.dq_mode)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
-    flops = case.flops()
+    flops = useful_flops(case)
     launches_per_step = 3 + (1 if args.dq_mode == 1 else 0) + (2 if case.total_kv > int(case.cu_kv[-1]) else 0)
-    input_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do, o, m, l, work.dq_acc))
+    input_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do, o, *stats, work.dq_acc))
 
     def step(ev=None):
         fab.fa_bwd_preprocess(o, do, work.D, work.dq_acc)
         if ev is not None:
             ev[0].record(stream)
-        fab.fa_bwd(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q, cu_kv, case.cu_q, case.cu_kv,
-                   case.causal, scale, args.dq_mode, work.ws)
+        if lse_stats:
+            fab.fa_bwd_lse(q, k, v, do, stats[0], work.D, work.dq_acc, dk, dv, cu_q, cu_kv, case.cu_q, case.cu_kv,
+                           mask, case.window, scale, args.dq_mode, work.ws)
+        else:
+            fab.fa_bwd_ex(q, k, v, do, *stats, work.D, work.dq_acc, dk, dv, cu_q, cu_kv, case.cu_q, case.cu_kv,
+                          mask, case.window, scale, args.dq_mode, work.ws)
         if ev is not None:
             ev[1].record(stream)
         fab.fa_bwd_dq_finalize(work.dq_acc, dq, scale)
@@ -320,9 +381,9 @@ def run_gpu(args):
     # end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        host_in = [t.cpu().pin_memory() for t in (q, k, v, o, do, m, l)]
+        host_in = [t.cpu().pin_memory() for t in (q, k, v, o, do, *stats)]
         host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
-        dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, m, l)]
+        dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, *stats)]
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
         n_e2e = max(3, min(args.steps, 20))
@@ -330,8 +391,9 @@ def run_gpu(args):
         def e2e_step():
             for d_, h_ in zip(dev_in, host_in):
                 d_.copy_(h_, non_blocking=True)
-            outs = fab.backward(*dev_in, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, args.dq_mode,
-                                out=(dq, dk, dv), work=work)
+            api = fab.backward_lse if lse_stats else fab.backward
+            outs = api(*dev_in, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, args.dq_mode,
+                       out=(dq, dk, dv), work=work, **mask_kw(case))
             for h_, d_ in zip(host_out, outs):
                 h_.copy_(d_, non_blocking=True)
 
@@ -357,7 +419,7 @@ def run_gpu(args):
     peak, hbm, peak_src = peaks()
     achieved = flops / (bwd_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "frac": achieved / peak, "traffic": None if lse_stats else profiled_traffic(args.workload),
                 "kernel": "fa_bwd (bwd_kernel<%d>)" % case.head_dim, "fa_bwd_ms": bwd_ms,
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
 
@@ -372,6 +434,7 @@ def run_gpu(args):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {workload_desc(case)}", "dq_mode": args.dq_mode,
+                   "statistics": "lse" if lse_stats else "m, l",
                    "l2": f"inputs larger than L2 ({input_bytes / 2**20:.0f} MiB resident per step)"
                    if input_bytes > L2_BYTES else "inputs smaller than L2",
                    "flops_per_step": flops},
@@ -393,7 +456,9 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="cfg3nc", choices=sorted(si.CONFIGS))
+    ap.add_argument("--workload", default="cfg3nc", choices=sorted(WORKLOADS))
+    ap.add_argument("--stats", choices=["ml", "lse"], default="ml",
+                    help="softmax statistics the backward consumes: (m, l) or lse = m + ln l")
     ap.add_argument("--dq-mode", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

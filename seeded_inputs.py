@@ -147,3 +147,24 @@ def cfg5() -> Case:
 
 CONFIGS = {"cfg1": cfg1, "cfg2": cfg2, "cfg3": lambda: cfg3(True),
            "cfg3nc": lambda: cfg3(False), "cfg4": cfg4, "cfg5": cfg5}
+
+
+# Workloads of the variants (grouped-query attention, masks): shapes of the
+# common uses, seeds 1100 + k.
+def gqa() -> Case:
+    """32 query heads sharing 8 key/value heads, causal, 4 x 4096 tokens."""
+    return fixed("gqa_b4_h32_hkv8_s4096_d128_causal", 4, 32, 128, 4096, 4096, True, 1101, heads_kv=8)
+
+
+def swa() -> Case:
+    """Causal sliding window of 4096 keys over 2 x 16384 tokens."""
+    return fixed("swa_b2_h16_s16384_w4096_d128", 2, 16, 128, 16384, 16384, True, 1102, window=4096)
+
+
+def br() -> Case:
+    """Bottom-right causal: 1024 new queries against 8192 keys (the last
+    1024 of them the queries' own), 8 sequences."""
+    return fixed("br_b8_h16_s1024_s8192_d128", 8, 16, 128, 1024, 8192, True, 1103, bottom_right=True)
+
+
+VARIANTS = {"gqa": gqa, "swa": swa, "br": br}
