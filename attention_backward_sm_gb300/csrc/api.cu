@@ -172,10 +172,21 @@ int fwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, f
   if (!q || !k || !v || !o || !m || (!stats_lse && !l) || !cu_q_dev || !cu_kv_dev)
     return fail(FA_ERR_INVALID_ARG, "a device pointer is NULL");
   if ((rc = check_device())) return rc;
-  fa::FwdParams p{};
-  p.q = q;
-  p.k = k;
-  p.v = v;
+  const void* al[] = {q, k, v, o};
+  for (const void* ptr : al)
+    if (!aligned16(ptr)) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  fa::FwdTcParams p;
+  memset(&p, 0, sizeof(p));
+  // With no key rows at all no key tile is ever loaded; the query tensor
+  // then stands in as a valid address for the (unused) key and value maps.
+  const bool no_keys = total_kv == 0;
+  if ((rc = make_map(&p.tm_q, q, total_q, heads, head_dim, "q"))) return rc;
+  if ((rc = make_map(&p.tm_k, no_keys ? static_cast<const void*>(q) : k, no_keys ? total_q : total_kv,
+                     no_keys ? heads : heads_kv, head_dim, "k")))
+    return rc;
+  if ((rc = make_map(&p.tm_v, no_keys ? static_cast<const void*>(q) : v, no_keys ? total_q : total_kv,
+                     no_keys ? heads : heads_kv, head_dim, "v")))
+    return rc;
   p.o = o;
   p.m = m;
   p.l = l;
@@ -188,8 +199,8 @@ int fwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, f
   p.window = effective_window(window, max_q, max_kv);
   p.stats_lse = stats_lse;
   p.scale = scale;
-  cudaError_t e = fa::launch_fwd_stats(p, head_dim, batch, (max_q + 63) / 64, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "fwd_stats launch");
+  cudaError_t e = fa::launch_fwd_main(p, head_dim, batch, (max_q + 127) / 128, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ok();
 }
 
@@ -417,11 +428,14 @@ int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads,
 }
 
 int fa_check_device_status(fa_stream_t stream) {
-  int st = 0;
+  int st = 0, st_fwd = 0;
   int e = fa::bwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st);
+  if (e == 0) e = fa::fwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st_fwd);
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "fa_check_device_status");
   if (st == 4) return fail(FA_ERR_TIMEOUT, "a device-side wait in fa_bwd ran out of time (status %d)", st);
   if (st != 0) return fail(FA_ERR_CUDA, "fa_bwd recorded device status %d", st);
+  if (st_fwd == 4) return fail(FA_ERR_TIMEOUT, "a device-side wait in the forward ran out of time (status %d)", st_fwd);
+  if (st_fwd != 0) return fail(FA_ERR_CUDA, "the forward recorded device status %d", st_fwd);
   return ok();
 }
 

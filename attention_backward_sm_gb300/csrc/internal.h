@@ -47,24 +47,26 @@ cudaError_t launch_preprocess(const uint16_t* o, const uint16_t* dout, float* D,
 cudaError_t launch_dq_finalize(const float* acc, uint16_t* dq, long long elems, float scale, cudaStream_t s);
 cudaError_t launch_zero_fill(void* p, long long bytes, cudaStream_t s);
 
-struct FwdParams {
-  const uint16_t* q;
-  const uint16_t* k;
-  const uint16_t* v;
+// Forward statistics on the tensor cores (fwd_main.cu).
+struct FwdTcParams {
+  CUtensorMap tm_q;    // [total_q, H*d] bf16, 128x64 boxes, 128-byte swizzle
+  CUtensorMap tm_k;    // [total_kv, Hkv*d]
+  CUtensorMap tm_v;
   uint16_t* o;
-  float* m;
+  float* m;            // m, or lse when stats_lse
   float* l;
   const int32_t* cu_q;
   const int32_t* cu_kv;
-  int heads;           // query heads
-  int heads_kv;        // key/value heads (heads is a multiple of it)
-  int causal;          // as in BwdParams
+  int heads;
+  int heads_kv;
+  int causal;
   int bottom_right;
   int window;
-  int stats_lse;       // 1: write lse = m + ln(l) into m and leave l untouched
+  int stats_lse;
   float scale;
 };
-cudaError_t launch_fwd_stats(const FwdParams& p, int head_dim, int batch, int max_q_blocks64, cudaStream_t s);
+cudaError_t launch_fwd_main(const FwdTcParams& p, int head_dim, int batch, int max_q_blocks, cudaStream_t s);
+int fwd_read_and_clear_status(cudaStream_t s, int* status);
 
 // Records a message for fa_last_error() on the calling thread and returns code.
 int set_last_error(int code, const char* fmt, ...);

@@ -81,7 +81,9 @@ enum fa_mask {
  * l and m).  Writes O = softmax(scale*QK^T) V (bf16), m_i = max_j of the
  * scaled scores and l_i = sum_j exp(scaled score - m_i) (float32) for every
  * row of every sequence.  Rows of a sequence with no keys get O = 0,
- * m = -inf, l = 0.  Padding rows are not written. */
+ * m = -inf, l = 0.  Padding rows are not written.  Runs on the tensor cores
+ * (one CTA per 128-row query block; O accumulates in tensor memory); q, k,
+ * v and o must be 16-byte aligned. */
 int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
                  fa_bf16* o, float* m, float* l,
                  const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
