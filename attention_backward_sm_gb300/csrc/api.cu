@@ -61,8 +61,8 @@ int check_shape(int batch, int total_q, int total_kv, int heads, int head_dim) {
   if (batch < 0) return fail(FA_ERR_INVALID_ARG, "batch must be >= 0, got %d", batch);
   if (heads < 1) return fail(FA_ERR_INVALID_ARG, "heads must be >= 1, got %d", heads);
   if (total_q < 0 || total_kv < 0) return fail(FA_ERR_INVALID_ARG, "total_q and total_kv must be >= 0");
-  if (head_dim != 64 && head_dim != 128)
-    return fail(FA_ERR_UNSUPPORTED, "head_dim must be 64 or 128, got %d", head_dim);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(FA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256, got %d", head_dim);
   if (static_cast<long long>(heads) * head_dim > 65535 * 64)
     return fail(FA_ERR_UNSUPPORTED, "heads * head_dim too large for a 2-D tensor map");
   return FA_OK;
@@ -105,17 +105,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A [rows, heads*head_dim] view with 128-byte swizzle: bf16 with 64 x 128
-// boxes (operand tiles; rows past `rows` read as zero), or fp32 with
-// 32 x 32 boxes (the dQ accumulator; rows past `rows` are not written).
+// A [rows, heads*head_dim] view with 128-byte swizzle: bf16 with boxes of
+// 64 columns x box_rows rows (operand tiles; rows past `rows` read as
+// zero), or fp32 with 32 x 32 boxes (the dQ accumulator; rows past `rows`
+// are not written).
 int make_map(CUtensorMap* m, const void* base, int rows, int heads, int head_dim, const char* name,
-             bool fp32 = false) {
+             bool fp32 = false, int box_rows = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t esize = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * head_dim, static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * head_dim * esize};
-  cuuint32_t box[2] = {fp32 ? 32u : 64u, fp32 ? 32u : 128u};
+  cuuint32_t box[2] = {fp32 ? 32u : 64u, fp32 ? 32u : static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -181,11 +182,12 @@ int fwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, f
   // then stands in as a valid address for the (unused) key and value maps.
   const bool no_keys = total_kv == 0;
   if ((rc = make_map(&p.tm_q, q, total_q, heads, head_dim, "q"))) return rc;
+  const int kv_box = head_dim == 256 ? 64 : 128;   // key rows per block of the forward kernel
   if ((rc = make_map(&p.tm_k, no_keys ? static_cast<const void*>(q) : k, no_keys ? total_q : total_kv,
-                     no_keys ? heads : heads_kv, head_dim, "k")))
+                     no_keys ? heads : heads_kv, head_dim, "k", false, kv_box)))
     return rc;
   if ((rc = make_map(&p.tm_v, no_keys ? static_cast<const void*>(q) : v, no_keys ? total_q : total_kv,
-                     no_keys ? heads : heads_kv, head_dim, "v")))
+                     no_keys ? heads : heads_kv, head_dim, "v", false, kv_box)))
     return rc;
   p.o = o;
   p.m = m;
@@ -275,8 +277,11 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   int max_q = 0;
   for (int b = 0; b < batch; ++b) max_q = cu_q_host[b + 1] - cu_q_host[b] > max_q ? cu_q_host[b + 1] - cu_q_host[b] : max_q;
   ok();
-  // one int32 counter per (batch, head, 128-row query block, 32-row quarter), rounded to 256 B
-  const size_t n = static_cast<size_t>(batch) * heads * ((max_q + 127) / 128) * 4;
+  // one int32 counter per (batch, head, 128-row query block, 32-row quarter); with
+  // head_dim 256 per (batch, head, 64-row query block, head-dim half, 32-dim quarter);
+  // rounded to 256 B
+  const size_t n = head_dim == 256 ? static_cast<size_t>(batch) * heads * ((max_q + 63) / 64) * 8
+                                   : static_cast<size_t>(batch) * heads * ((max_q + 127) / 128) * 4;
   return ((n * 4 + 255) / 256) * 256;
 }
 
@@ -331,12 +336,14 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
   // then stands in as a valid address for the (unused) query maps.
   const void* qbase = max_q > 0 ? static_cast<const void*>(q) : static_cast<const void*>(k);
   const void* dobase = max_q > 0 ? static_cast<const void*>(dout) : static_cast<const void*>(k);
-  if ((rc = make_map(&p.tm_q, qbase, max_q > 0 ? total_q : total_kv, max_q > 0 ? heads : heads_kv, head_dim, "q")))
+  const int q_box = head_dim == 256 ? 64 : 128;   // query rows per block of the backward kernel
+  if ((rc = make_map(&p.tm_q, qbase, max_q > 0 ? total_q : total_kv, max_q > 0 ? heads : heads_kv, head_dim, "q",
+                     false, q_box)))
     return rc;
   if ((rc = make_map(&p.tm_k, k, total_kv, heads_kv, head_dim, "k"))) return rc;
   if ((rc = make_map(&p.tm_v, v, total_kv, heads_kv, head_dim, "v"))) return rc;
   if ((rc = make_map(&p.tm_do, dobase, max_q > 0 ? total_q : total_kv, max_q > 0 ? heads : heads_kv, head_dim,
-                     "dout")))
+                     "dout", false, q_box)))
     return rc;
   if (max_q > 0 && (rc = make_map(&p.tm_dq, dq_acc, total_q, heads, head_dim, "dq_acc", true))) return rc;
   p.m = m;
@@ -354,7 +361,7 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
   p.window = effective_window(window, max_q, max_kv);
   p.stats_lse = stats_lse;
   p.dq_mode = dq_mode;
-  p.max_q_blocks = (max_q + 127) / 128;
+  p.max_q_blocks = (max_q + q_box - 1) / q_box;
   p.kv_reverse = (dq_mode == FA_DQ_DETERMINISTIC && causal) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -363,7 +370,8 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
     cudaError_t e = fa::launch_zero_fill(workspace, static_cast<long long>(need), s);
     if (e != cudaSuccess) return cuda_fail(e, "ticket reset");
   }
-  cudaError_t e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, s);
+  cudaError_t e = head_dim == 256 ? fa::launch_bwd256(p, batch, (max_kv + 127) / 128, s)
+                                   : fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, s);
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
   return ok();
 }
@@ -428,9 +436,11 @@ int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads,
 }
 
 int fa_check_device_status(fa_stream_t stream) {
-  int st = 0, st_fwd = 0;
+  int st = 0, st256 = 0, st_fwd = 0;
   int e = fa::bwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st);
+  if (e == 0) e = fa::bwd256_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st256);
   if (e == 0) e = fa::fwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st_fwd);
+  if (st == 0) st = st256;
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "fa_check_device_status");
   if (st == 4) return fail(FA_ERR_TIMEOUT, "a device-side wait in fa_bwd ran out of time (status %d)", st);
   if (st != 0) return fail(FA_ERR_CUDA, "fa_bwd recorded device status %d", st);

@@ -42,11 +42,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int BQ = 128;                  // query rows per CTA
-constexpr int BK = 128;                  // key rows per block
-constexpr uint32_t CHUNK = 128 * 128;    // one TMA box: 128 rows x 64 bf16
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S0 = 0;           // two S buffers of 128 columns
-constexpr uint32_t COL_O = 256;
+constexpr uint32_t COL_S0 = 0;           // two S buffers of BK columns, then O (d columns)
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (factor 256)
 
 enum {
@@ -54,23 +51,35 @@ enum {
   B_S_FULL0, B_S_FULL1, B_P_READY, B_O_DONE, B_TEARDOWN, NUM_BARS
 };
 
+// Tiles are stored as 64-column (128-byte) chunks of `rows` rows each, as
+// TMA writes them with 128-byte swizzle.  With d = 256 the key blocks are
+// 64 rows, so that Q (128 x 256) and two stages of K and V fit in shared
+// memory and O (256 columns) fits in TMEM beside the two score buffers.
 template <int D>
 struct Layout {
-  static constexpr uint32_t TILE = 128 * D * 2;
+  static constexpr int BK = (D == 256) ? 64 : 128;   // key rows per block
+  static constexpr uint32_t CHUNK_Q = 128 * 128;      // 128 rows x 128 B
+  static constexpr uint32_t CHUNK_KV = BK * 128;
+  static constexpr uint32_t TILE_Q = 128 * D * 2;
+  static constexpr uint32_t TILE_KV = BK * D * 2;
   static constexpr int NCH = D / 64;
   static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K = TILE;          // 2 stages
-  static constexpr uint32_t V = 3 * TILE;      // 2 stages
-  static constexpr uint32_t BARS = 5 * TILE;
+  static constexpr uint32_t K = TILE_Q;                // 2 stages
+  static constexpr uint32_t V = TILE_Q + 2 * TILE_KV;  // 2 stages
+  static constexpr uint32_t BARS = TILE_Q + 4 * TILE_KV;
   static constexpr uint32_t MISC = BARS + NUM_BARS * 8;
   static constexpr uint32_t BYTES = MISC + 16;
+  static constexpr uint32_t COL_O = 2 * BK;
+  static_assert(COL_O + D <= TMEM_COLS, "tensor memory budget");
 };
 
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int t) {
-  return sw128_desc(tile + (t >> 2) * CHUNK + (t & 3) * 32, 16, 1024);
+// 16-element K step t of a K-major tile stored in chunks of `chunk` bytes
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int t, uint32_t chunk) {
+  return sw128_desc(tile + (t >> 2) * chunk + (t & 3) * 32, 16, 1024);
 }
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int t) {
-  return sw128_desc(tile + t * 2048, CHUNK, 1024);
+// rows 16t..16t+15 of an MN-major tile whose 64-column chunks are `chunk` apart
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int t, uint32_t chunk) {
+  return sw128_desc(tile + t * 2048, chunk, 1024);
 }
 
 __device__ __forceinline__ int floordiv(long long a, int b) {
@@ -89,6 +98,7 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdTcParams p) {
   using L = Layout<D>;
+  constexpr int BK = L::BK;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
@@ -170,9 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(bar(B_Q_FULL), L::TILE);
+      mbar_arrive_expect_tx(bar(B_Q_FULL), L::TILE_Q);
       for (int c = 0; c < L::NCH; ++c)
-        tma_load_2d(sbase + L::Q + c * CHUNK, &p.tm_q, h * D + c * 64, q_start + qb * BQ, bar(B_Q_FULL));
+        tma_load_2d(sbase + L::Q + c * L::CHUNK_Q, &p.tm_q, h * D + c * 64, q_start + qb * BQ, bar(B_Q_FULL));
     }
     __syncwarp();
     // The producer only issues loads: the MMA warp waits for their arrival
@@ -183,10 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       if (j >= 2 && !mbar_wait(bar(B_KV_EMPTY0 + s), ((j >> 1) - 1) & 1, abort, status)) { ok = false; break; }
       if (lane == 0) {
         const int row = kv_start + (kb0 + j) * BK;
-        mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), 2 * L::TILE);
+        mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), 2 * L::TILE_KV);
         for (int c = 0; c < L::NCH; ++c) {
-          tma_load_2d(sbase + L::K + s * L::TILE + c * CHUNK, &p.tm_k, hk * D + c * 64, row, bar(B_KV_FULL0 + s));
-          tma_load_2d(sbase + L::V + s * L::TILE + c * CHUNK, &p.tm_v, hk * D + c * 64, row, bar(B_KV_FULL0 + s));
+          tma_load_2d(sbase + L::K + s * L::TILE_KV + c * L::CHUNK_KV, &p.tm_k, hk * D + c * 64, row,
+                      bar(B_KV_FULL0 + s));
+          tma_load_2d(sbase + L::V + s * L::TILE_KV + c * L::CHUNK_KV, &p.tm_v, hk * D + c * 64, row,
+                      bar(B_KV_FULL0 + s));
         }
       }
       __syncwarp();
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     mbar_wait(bar(B_Q_FULL), 0, &no_abort, status);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);   // S = Q K^T, both K-major
+    constexpr uint32_t ID_S = idesc_bf16(128, BK, 0, 0);    // S = Q K^T, both K-major
     constexpr uint32_t ID_O = idesc_bf16(128, D, 0, 1);     // O += P V, V (B) MN-major
     const uint32_t sQ = sbase + L::Q;
     bool ok = mbar_wait(bar(B_Q_FULL), 0, abort, status) && mbar_wait(bar(B_KV_FULL0), 0, abort, status);
@@ -207,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       if (elect_one()) {
 #pragma unroll 1
         for (int t = 0; t < D / 16; ++t)
-          mma_ss(tmem + COL_S0, desc_kmajor(sQ, t), desc_kmajor(sbase + L::K, t), ID_S, t > 0);
+          mma_ss(tmem + COL_S0, desc_kmajor(sQ, t, L::CHUNK_Q), desc_kmajor(sbase + L::K, t, L::CHUNK_KV), ID_S,
+                 t > 0);
         mma_commit(bar(B_S_FULL0));
       }
       __syncwarp();
@@ -221,10 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         if (j >= 1 && !mbar_wait(bar(B_O_DONE), (j - 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t sK = sbase + L::K + s1n * L::TILE;
+          const uint32_t sK = sbase + L::K + s1n * L::TILE_KV;
 #pragma unroll 1
           for (int t = 0; t < D / 16; ++t)
-            mma_ss(tmem + COL_S0 + s1n * 128, desc_kmajor(sQ, t), desc_kmajor(sK, t), ID_S, t > 0);
+            mma_ss(tmem + COL_S0 + s1n * BK, desc_kmajor(sQ, t, L::CHUNK_Q), desc_kmajor(sK, t, L::CHUNK_KV), ID_S,
+                   t > 0);
           mma_commit(bar(B_S_FULL0 + s1n));
         }
         __syncwarp();
@@ -232,10 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       if (!mbar_wait(bar(B_P_READY), j & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       if (elect_one()) {
-        const uint32_t sV = sbase + L::V + s * L::TILE;
+        const uint32_t sV = sbase + L::V + s * L::TILE_KV;
 #pragma unroll 1
         for (int t = 0; t < BK / 16; ++t)
-          mma_ts(tmem + COL_O, tmem + COL_S0 + s * 128 + t * 8, desc_mnmajor(sV, t), ID_O, (j > 0) | (t > 0));
+          mma_ts(tmem + L::COL_O, tmem + COL_S0 + s * BK + t * 8, desc_mnmajor(sV, t, L::CHUNK_KV), ID_O,
+                 (j > 0) | (t > 0));
         mma_commit(bar(B_O_DONE));
         mma_commit(bar(B_KV_EMPTY0 + s));
       }
@@ -273,12 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || span < BK);
       if (!mbar_wait(bar(B_S_FULL0 + s), (j >> 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t t_s = tmem + lane_addr + COL_S0 + s * 128;
-      float x[128];
+      const uint32_t t_s = tmem + lane_addr + COL_S0 + s * BK;
+      float x[BK];
       {
         uint32_t v[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < BK / 32; ++c) {
           tmem_ld32(t_s + c * 32, v);
           tmem_ld_wait();
 #pragma unroll
@@ -287,12 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       }
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < BK; ++c)
           x[c] = (static_cast<unsigned>(c - c_lo) < static_cast<unsigned>(span)) ? x[c] : -INFINITY;
       }
       float mx = x[0];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      for (int c = 1; c < BK; ++c) mx = fmaxf(mx, x[c]);
       mx_raw = fmaxf(mx_raw, mx);
       const float m_new = fmaxf(m_used, mx * sl2);
       const bool grow = m_new > m_used + kRescaleLog2;   // also true for the first visible key
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + COL_O + c * 32, v);
+          tmem_ld32(tmem + lane_addr + L::COL_O + c * 32, v);
           tmem_ld_wait();
           uint32_t w0[16], w1[16];
 #pragma unroll
@@ -319,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             w0[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
             w1[e] = __float_as_uint(__uint_as_float(v[16 + e]) * alpha);
           }
-          tmem_st16(tmem + lane_addr + COL_O + c * 32, w0);
-          tmem_st16(tmem + lane_addr + COL_O + c * 32 + 16, w1);
+          tmem_st16(tmem + lane_addr + L::COL_O + c * 32, w0);
+          tmem_st16(tmem + lane_addr + L::COL_O + c * 32 + 16, w1);
         }
         tmem_st_wait();
       }
@@ -330,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       // P = 2^(x*sl2 - m_used), masked entries (x = -inf) give 0
       float sum = 0.f;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < BK / 32; ++g) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -348,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         // P = 0 does not cancel a NaN: zero them before O += P V reads them
         // (the scores of those key rows are masked, so K needs no fix-up)
         if (!mbar_wait(bar(B_KV_FULL0 + s), (j >> 1) & 1, abort, status)) { ok = false; break; }
-        const uint32_t sV = sbase + L::V + s * L::TILE;
+        const uint32_t sV = sbase + L::V + s * L::TILE_KV;
         constexpr int G16 = D / 8;   // 16-byte granules per row
         for (int e = r; e < (BK - kv_valid) * G16; e += 128) {
           const int row = kv_valid + e / G16, g = e % G16;
-          st_shared_v4(sV + (g / 8) * CHUNK + row * 128 + (g % 8) * 16, 0u, 0u, 0u, 0u);
+          st_shared_v4(sV + (g / 8) * L::CHUNK_KV + row * 128 + (g % 8) * 16, 0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
       }
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_addr + COL_O + c * 32, v);
+        tmem_ld32(tmem + lane_addr + L::COL_O + c * 32, v);
         tmem_ld_wait();
         if (r < q_valid) {
           uint32_t pk[16];
@@ -422,7 +437,9 @@ cudaError_t launch_d(const FwdTcParams& p, int batch, int max_q_blocks, cudaStre
 
 cudaError_t launch_fwd_main(const FwdTcParams& p, int head_dim, int batch, int max_q_blocks, cudaStream_t s) {
   if (batch <= 0 || max_q_blocks <= 0) return cudaSuccess;
-  return head_dim == 64 ? launch_d<64>(p, batch, max_q_blocks, s) : launch_d<128>(p, batch, max_q_blocks, s);
+  if (head_dim == 64) return launch_d<64>(p, batch, max_q_blocks, s);
+  if (head_dim == 256) return launch_d<256>(p, batch, max_q_blocks, s);
+  return launch_d<128>(p, batch, max_q_blocks, s);
 }
 
 int fwd_read_and_clear_status(cudaStream_t s, int* status) {

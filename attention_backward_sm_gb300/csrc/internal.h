@@ -40,6 +40,9 @@ struct BwdParams {
 };
 
 cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, cudaStream_t s);
+// head_dim 256 (bwd_d256.cu): tm_q / tm_do with 64-row boxes, max_q_blocks in 64-row blocks
+cudaError_t launch_bwd256(const BwdParams& p, int batch, int max_kv_blocks, cudaStream_t s);
+int bwd256_read_and_clear_status(cudaStream_t s, int* status);
 int bwd_read_and_clear_status(cudaStream_t s, int* status);
 
 cudaError_t launch_preprocess(const uint16_t* o, const uint16_t* dout, float* D, float* dq_acc, long long rows,

@@ -122,6 +122,8 @@ cudaError_t launch_preprocess(const uint16_t* o, const uint16_t* dout, float* D,
   const int grid = grid_for(lanes);
   if (head_dim == 64)
     preprocess_kernel<64><<<grid, kThreads, 0, s>>>(o, dout, D, dq_acc, rows);
+  else if (head_dim == 256)
+    preprocess_kernel<256><<<grid, kThreads, 0, s>>>(o, dout, D, dq_acc, rows);
   else
     preprocess_kernel<128><<<grid, kThreads, 0, s>>>(o, dout, D, dq_acc, rows);
   return cudaGetLastError();

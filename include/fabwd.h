@@ -27,7 +27,8 @@
  *     hold the same values: the host copy sizes the launch.
  *   - All device pointers are caller-owned device memory, 16-byte aligned.
  *     The library allocates no device memory on these paths.
- *   - head_dim must be 64 or 128; heads >= 1.
+ *   - head_dim must be 64, 128 or 256 (the JAX cuDNN wrapper's
+ *     check_is_flash_attention admits head dims up to 256); heads >= 1.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
  *     default stream) and returns FA_OK or an error code.  Arguments are
  *     checked on the host before anything is launched; on an error nothing
@@ -52,7 +53,7 @@ typedef struct CUstream_st* fa_stream_t;  /* same type as cudaStream_t */
 enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,   /* null pointer, bad offsets, bad sizes, misalignment */
-    FA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, no sm_103a device */
+    FA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128, 256}, no sm_103a device */
     FA_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
     FA_ERR_TIMEOUT = 4        /* a device-side bounded wait ran out */
 };
@@ -181,6 +182,14 @@ int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf
                int batch, int total_q, int total_kv, int heads, int heads_kv, int head_dim,
                int causal, float scale, int dq_mode,
                void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* head_dim 256: the dK and dV accumulators of a 128-row key block would
+ * fill the whole tensor memory, so two CTAs share each (sequence, key/value
+ * head, key block), one per half of the head dimension; each computes the
+ * full scores and dP (7/5 of the minimum matmul work) and its half of dK,
+ * dV and dQ, over 64-row query blocks.  In FA_DQ_DETERMINISTIC mode the
+ * workspace then holds one counter per (batch, head, 64-row query block,
+ * head-dim half, 32-dim quarter); fa_bwd_workspace_size accounts for it. */
 
 /* fa_bwd_gqa with a mask and a sliding window (as in fa_fwd_stats_ex).
  * A CTA visits only the query blocks whose tiles the band of visible

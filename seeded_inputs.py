@@ -167,4 +167,10 @@ def br() -> Case:
     return fixed("br_b8_h16_s1024_s8192_d128", 8, 16, 128, 1024, 8192, True, 1103, bottom_right=True)
 
 
-VARIANTS = {"gqa": gqa, "swa": swa, "br": br}
+def d256(causal: bool = False) -> Case:
+    """head_dim 256, 4 x 4096 tokens, 8 heads (the FLOPs of cfg3)."""
+    name = "d256_b4_h8_s4096_" + ("causal" if causal else "noncausal")
+    return fixed(name, 4, 8, 256, 4096, 4096, causal, 1104)
+
+
+VARIANTS = {"gqa": gqa, "swa": swa, "br": br, "d256": lambda: d256(False), "d256c": lambda: d256(True)}
