@@ -33,13 +33,15 @@
 // warps 0-3, 152 for the softmax warpgroups, 152 for the write-back, which
 // holds a whole 128-column dQ partial; the sum, 64512, fits the 65536 the
 // block is launched with):
-//   warp 0      TMA producer: K, V once; Q, dO and per-row stats per block
+//   warp 0      TMA producer: K, V once; Q and per-row stats per block
 //               (2-stage ring); zeroes rows past a sequence end
+//   warp 2      TMA producer of dO (2-stage ring), independent of warp 0
 //   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
 //   warps 4-11  two softmax warpgroups, each owning 64 of the 128 query
 //               columns for all 128 key rows; at the end dV (4-7), dK (8-11)
-//   warps 12-15 dQ write-back: TMEM -> shared memory (half in the dS
-//               buffer, half in the block's own dO buffer) -> TMA reduce-add
+//   warps 12-15 dQ write-back: TMEM -> shared memory (buffers the MMAs are
+//               done with: the block's dO and Q (d = 128) or dS (d = 64)
+//               buffers) -> TMA reduce-add
 // Every mbarrier wait is bounded (see sm103.cuh); on a timeout the CTA
 // records FA_ERR_TIMEOUT in the status word, drains and frees TMEM.
 #include <cuda.h>
@@ -59,7 +61,7 @@ constexpr int kThreads = 512;
 // Registers per thread: the block launches with 65536 / 512 = 128 and each
 // warpgroup then moves to its own budget.
 constexpr uint32_t kRegLaunch = 65536 / kThreads;
-constexpr uint32_t kRegOther = 48;     // warps 0-3: producer, MMA issuer, two idle warps
+constexpr uint32_t kRegOther = 48;     // warps 0-3: producers, MMA issuer, one idle warp
 constexpr uint32_t kRegSoftmax = 152;  // warps 4-11
 constexpr uint32_t kRegDrain = 152;    // warps 12-15
 static_assert(128 * kRegOther + 256 * kRegSoftmax + 128 * kRegDrain <= 65536, "register budgets exceed the launch");
@@ -79,6 +81,14 @@ enum {
   B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
   B_TEARDOWN, NUM_BARS
 };
+
+// Where the first half of a dQ partial is staged on its way to TMA: with
+// d = 128 in the block's own Q buffer (so the dS buffer is free as soon as
+// dK / dQ have run), with d = 64 in the dS buffer (measured faster there:
+// the d = 64 kernel is bound by the softmax, and releasing Q later costs
+// more than the dS hand-off).
+template <int D>
+constexpr bool kStageInQ = (D == 128);
 
 template <int D>
 struct Layout {
@@ -303,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_Q_FULL0 + s), 1);
       mbar_init(bar(B_Q_READY0 + s), 1);
-      mbar_init(bar(B_Q_EMPTY0 + s), 1);
+      mbar_init(bar(B_Q_EMPTY0 + s), kStageInQ<D> ? 4 : 1);   // write-back warps, or the MMA commit
       mbar_init(bar(B_DO_FULL0 + s), 1);
       mbar_init(bar(B_DO_READY0 + s), 1);
       mbar_init(bar(B_DO_EMPTY0 + s), 4);   // one arrive per dQ write-back warp
@@ -313,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     mbar_init(bar(B_P_READY), 256);
     mbar_init(bar(B_P_USED), 1);
     mbar_init(bar(B_DS_READY), 256);
-    mbar_init(bar(B_DS_FREE), 4);     // one arrive per dQ write-back warp
+    mbar_init(bar(B_DS_FREE), kStageInQ<D> ? 1 : 4);
     mbar_init(bar(B_DQ_FULL), 1);
     mbar_init(bar(B_DQ_EMPTY), 128);
     mbar_init(bar(B_ACC_FULL), 1);
@@ -348,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       __syncwarp();
       // Loads issued but not yet seen complete must land before the CTA
       // exits, even on the abort path: remember their barriers and parities.
-      int pend_kv = 1, pend_q = -1, pend_do = -1;
-      uint32_t par_q = 0, par_do = 0;
+      int pend_kv = 1, pend_q = -1;
+      uint32_t par_q = 0;
       bool ok = mbar_wait(bar(B_KV_FULL), 0, abort, status);
       if (ok) {
         pend_kv = 0;
@@ -382,16 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
       };
       load_stats(0, nm, nl, nd);
+      // Q (with the row statistics) here; dO has a producer warp of its own,
+      // so that each stream's load is issued as soon as its stage is free:
+      // loads share the SM's TMA engine with the dQ reduce-adds and take
+      // over a thousand cycles to land.
       for (int k = 0; ok && k < n_it; ++k) {
         const int s = k & 1;
         const uint32_t prev = ((k >> 1) - 1) & 1;   // parity of this stage's previous release
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          rm[j] = nm[j];
-          rl[j] = nl[j];
-          rd[j] = nd[j];
-        }
-        load_stats(k + 1, nm, nl, nd);
         const int qb = qb_of(k);
         const int hq = hq_of(k);
         const int q_row0 = q_start + qb * BN;
@@ -406,6 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         par_q = (k >> 1) & 1;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          rm[j] = nm[j];
+          rl[j] = nl[j];
+          rd[j] = nd[j];
+        }
+        load_stats(k + 1, nm, nl, nd);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
           // log2 of the softmax denominator, exp(x - m) / l = 2^(x*log2e - lse2)
           st_lse[s * 128 + lane + 32 * j] = rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j]));
           st_D[s * 128 + lane + 32 * j] = rd[j];
@@ -418,12 +432,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
+      }
+      volatile int no_abort = 0;
+      if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
+      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dO producer
+    setmaxnreg_to<kRegOther, kRegLaunch>();
+    if (n_it > 0) {
+      int pend_do = -1;
+      uint32_t par_do = 0;
+      for (int k = 0; k < n_it; ++k) {
+        const int s = k & 1;
+        const uint32_t prev = ((k >> 1) - 1) & 1;
+        const int qb = qb_of(k);
+        const int q_valid = min(BN, s1 - qb * BN);
         if (k >= 2 && !mbar_wait(bar(B_DO_EMPTY0 + s), prev, abort, status)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_DO_FULL0 + s), L::TILE);
           for (int c = 0; c < L::NCH; ++c)
-            tma_load_2d(sbase + L::DO + s * L::TILE + c * CHUNK, &p.tm_do, hq * D + c * 64, q_row0,
-                        bar(B_DO_FULL0 + s));
+            tma_load_2d(sbase + L::DO + s * L::TILE + c * CHUNK, &p.tm_do, hq_of(k) * D + c * 64,
+                        q_start + qb * BN, bar(B_DO_FULL0 + s));
         }
         pend_do = s;
         par_do = (k >> 1) & 1;
@@ -437,8 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (lane == 0) mbar_arrive(bar(B_DO_READY0 + s));
       }
       volatile int no_abort = 0;
-      if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
-      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
       if (pend_do >= 0) mbar_wait(bar(B_DO_FULL0 + pend_do), par_do, &no_abort, status);
     }
   } else if (warp == 1) {
@@ -512,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                 mmas_km(t_dk, sDS, sQ, ID_KV, BN / 16, k > 0);
                 mmas_mm(t_dp, sDS, sK, ID_DQ, BM / 16, 0);
                 mma_commit(bar(B_DQ_FULL));
-                mma_commit(bar(B_Q_EMPTY0 + s));
+                mma_commit(bar(kStageInQ<D> ? B_DS_FREE : B_Q_EMPTY0 + s));
               }
               __syncwarp();
               need_c2 = false;
@@ -588,8 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 #pragma unroll
       for (int i = 0; i < 8; ++i) dv4v[i] = dvec4[i];
       if (!mbar_wait(bar(B_DP_FULL), ph, abort, status)) { ok = false; break; }
-      // The dS buffer holds half of the previous block's dQ staging until
-      // its TMA reduce has read it (which is after dK / dQ consumed dS).
+      // The dS buffer is free once the previous block's dK / dQ MMAs ran
+      // (d = 128) or once TMA has read the dQ half staged in it (d = 64).
       if (k > 0 && !mbar_wait(bar(B_DS_FREE), (k - 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t ds_row = sbase + L::DS + wg * CHUNK + (r >> 3) * 1024 + (r & 7) * 128;
@@ -635,11 +663,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     setmaxnreg_to<kRegDrain, kRegLaunch>();
     // TMEM lanes are query rows.  The partial of block k leaves as
     // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
-    // First half of the columns: staged in the dS buffer (free once dK_k and
-    // dQ_k have run), released to the softmax warps as soon as TMA has read
-    // it.  Second half: staged in block k's dO buffer (dead after dV_k),
-    // released to the producer afterwards.  Both halves are in flight at
-    // once; the SM's write-out bandwidth, not the staging, sets the pace.
+    // First half of the columns: staged in block k's Q buffer (d = 128; dead
+    // once dK_k has run, so the dS buffer is free for the next dS as soon as
+    // dK_k and dQ_k complete) or in the dS buffer (d = 64); second half in
+    // block k's dO buffer (dead after dV_k).  Each is released to its owner
+    // once TMA has read it.  Both halves are in flight at once; the SM's
+    // write-out bandwidth sets the pace.
     const int quarter = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr int NC = D / 32;              // 32-column chunks: 2 or 4
@@ -657,12 +686,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     // the head was launched before this one and never waits on a later one.
     const bool det = p.dq_mode != 0;
     bool issued = false;
-    const uint32_t slot_a = sbase + L::DS + quarter * 8192;            // up to two 4 KB boxes per warp
+
     for (int k = 0; k < n_it; ++k) {
       const int s = k & 1;
       const int qb = qb_of(k);
       const int hq = hq_of(k);
       const int y = q_start + qb * BN + quarter * 32;
+      // The partial is staged in this block's own dO buffer and (d = 128)
+      // Q buffer or (d = 64) the dS buffer, none of which the MMAs read once
+      // dQ_i is complete; each goes back to its owner once TMA has read it.
+      const uint32_t slot_a = kStageInQ<D> ? sbase + L::Q + s * L::TILE + quarter * (L::TILE / 4)
+                                           : sbase + L::DS + quarter * 8192;
       const uint32_t slot_b = sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
       int* ticket = det ? p.tickets + (static_cast<long long>(b * H + hq) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
       if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
@@ -718,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         bulk_commit();
         asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
-        mbar_arrive(bar(B_DS_FREE));
+        mbar_arrive(bar(kStageInQ<D> ? B_Q_EMPTY0 + s : B_DS_FREE));
         bulk_wait_read0();                                               // second half read
         mbar_arrive(bar(B_DO_EMPTY0 + s));
         if (det) {
@@ -733,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     }
     if (lane == 0 && issued) bulk_wait_all0();
   } else {
-    setmaxnreg_to<kRegOther, kRegLaunch>();   // warps 2 and 3 only wait at the final barrier
+    setmaxnreg_to<kRegOther, kRegLaunch>();   // warp 3 only waits at the final barrier
   }
 
   tc_fence_before();
