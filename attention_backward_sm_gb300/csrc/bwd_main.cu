@@ -29,9 +29,9 @@
 // dK_i, dQ_i: the next block's scores are computed while the softmax
 // warps derive dS_i.
 //
-// Warp roles (512 threads; registers per thread set per warpgroup: 48 for
+// Warp roles (512 threads; registers per thread set per warpgroup: 56 for
 // warps 0-3, 152 for the softmax warpgroups, 152 for the write-back, which
-// holds a whole 128-column dQ partial; the sum, 64512, fits the 65536 the
+// holds a whole 128-column dQ partial; the sum is exactly the 65536 the
 // block is launched with):
 //   warp 0      TMA producer: K, V once; Q and per-row stats per block
 //               (2-stage ring); zeroes rows past a sequence end
@@ -61,7 +61,7 @@ constexpr int kThreads = 512;
 // Registers per thread: the block launches with 65536 / 512 = 128 and each
 // warpgroup then moves to its own budget.
 constexpr uint32_t kRegLaunch = 65536 / kThreads;
-constexpr uint32_t kRegOther = 48;     // warps 0-3: producers, MMA issuer, one idle warp
+constexpr uint32_t kRegOther = 56;     // warps 0-3: producers, MMA issuer, one idle warp
 constexpr uint32_t kRegSoftmax = 152;  // warps 4-11
 constexpr uint32_t kRegDrain = 152;    // warps 12-15
 static_assert(128 * kRegOther + 256 * kRegSoftmax + 128 * kRegDrain <= 65536, "register budgets exceed the launch");
@@ -115,27 +115,39 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int t) {
   return sw128_desc(tile + t * 2048, CHUNK, 1024);
 }
 
-// MMA groups over n 16-element K steps, issued by one thread.  The loops are
-// kept rolled: the issuing warp runs on a small register budget.
+// MMA groups over N 16-element K steps, issued by one thread.  The
+// descriptors of a group are built once and stepped by constants (the start
+// address sits in the descriptor's low 14 bits as addr >> 4, and every step
+// stays inside the tile), so each MMA costs the issuing warp a 64-bit add.
 // acc: whether the first step accumulates into D.
-__device__ __forceinline__ void mmas_kk(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
-#pragma unroll 1
-  for (int t = 0; t < n; ++t) mma_ss(d, desc_kmajor(a_tile, t), desc_kmajor(b_tile, t), idesc, acc | (t > 0));
+__device__ __forceinline__ constexpr uint64_t step_kmajor(int t) { return ((t >> 2) * CHUNK + (t & 3) * 32) >> 4; }
+__device__ __forceinline__ constexpr uint64_t step_mnmajor(int t) { return (t * 2048) >> 4; }
+template <int N>
+__device__ __forceinline__ void mmas_kk(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, uint32_t acc) {
+  const uint64_t a0 = desc_kmajor(a_tile, 0), b0 = desc_kmajor(b_tile, 0);
+#pragma unroll 4
+  for (int t = 0; t < N; ++t) mma_ss(d, a0 + step_kmajor(t), b0 + step_kmajor(t), idesc, acc | (t > 0));
 }
-__device__ __forceinline__ void mmas_km(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
-#pragma unroll 1
-  for (int t = 0; t < n; ++t) mma_ss(d, desc_kmajor(a_tile, t), desc_mnmajor(b_tile, t), idesc, acc | (t > 0));
+template <int N>
+__device__ __forceinline__ void mmas_km(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, uint32_t acc) {
+  const uint64_t a0 = desc_kmajor(a_tile, 0), b0 = desc_mnmajor(b_tile, 0);
+#pragma unroll 4
+  for (int t = 0; t < N; ++t) mma_ss(d, a0 + step_kmajor(t), b0 + step_mnmajor(t), idesc, acc | (t > 0));
 }
-__device__ __forceinline__ void mmas_mm(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
-#pragma unroll 1
-  for (int t = 0; t < n; ++t) mma_ss(d, desc_mnmajor(a_tile, t), desc_mnmajor(b_tile, t), idesc, acc | (t > 0));
+template <int N>
+__device__ __forceinline__ void mmas_mm(uint32_t d, uint32_t a_tile, uint32_t b_tile, uint32_t idesc, uint32_t acc) {
+  const uint64_t a0 = desc_mnmajor(a_tile, 0), b0 = desc_mnmajor(b_tile, 0);
+#pragma unroll 4
+  for (int t = 0; t < N; ++t) mma_ss(d, a0 + step_mnmajor(t), b0 + step_mnmajor(t), idesc, acc | (t > 0));
 }
 // A from TMEM: P of K step t sits at column 64*(t/4) + 8*(t%4) (each softmax
 // warpgroup keeps its 64 query columns' P in the first 32 of its 64 columns).
-__device__ __forceinline__ void mmas_tm(uint32_t d, uint32_t a_tmem, uint32_t b_tile, uint32_t idesc, int n, uint32_t acc) {
-#pragma unroll 1
-  for (int t = 0; t < n; ++t)
-    mma_ts(d, a_tmem + (t >> 2) * 64 + (t & 3) * 8, desc_mnmajor(b_tile, t), idesc, acc | (t > 0));
+template <int N>
+__device__ __forceinline__ void mmas_tm(uint32_t d, uint32_t a_tmem, uint32_t b_tile, uint32_t idesc, uint32_t acc) {
+  const uint64_t b0 = desc_mnmajor(b_tile, 0);
+#pragma unroll 4
+  for (int t = 0; t < N; ++t)
+    mma_ts(d, a_tmem + (t >> 2) * 64 + (t & 3) * 8, b0 + step_mnmajor(t), idesc, acc | (t > 0));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -484,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       if (ok) {
         tc_fence_after();
         if (elect_one()) {
-          mmas_kk(t_s, sK, sbase + L::Q, ID_S, D / 16, 0);
+          mmas_kk<D / 16>(t_s, sK, sbase + L::Q, ID_S, 0);
           mma_commit(bar(B_S_FULL));
         }
         __syncwarp();
@@ -498,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (!mbar_wait(bar(B_DO_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-          mmas_kk(t_dp, sV, sDO, ID_S, D / 16, 0);
+          mmas_kk<D / 16>(t_dp, sV, sDO, ID_S, 0);
           mma_commit(bar(B_DP_FULL));
         }
         __syncwarp();
@@ -506,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (!mbar_wait(bar(B_P_READY), ph, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-          mmas_tm(t_dv, t_s, sDO, ID_KV, BN / 16, k > 0);
+          mmas_tm<BN / 16>(t_dv, t_s, sDO, ID_KV, k > 0);
           mma_commit(bar(B_P_USED));
         }
         __syncwarp();
@@ -528,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             if (s_ready && !c_ready) {
               tc_fence_after();
               if (elect_one()) {
-                mmas_kk(t_s, sK, sbase + L::Q + s1n * L::TILE, ID_S, D / 16, 0);
+                mmas_kk<D / 16>(t_s, sK, sbase + L::Q + s1n * L::TILE, ID_S, 0);
                 mma_commit(bar(B_S_FULL));
               }
               __syncwarp();
@@ -537,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
               // dK += dS^T Q and the dQ partial, both from dS in shared memory.
               tc_fence_after();
               if (elect_one()) {
-                mmas_km(t_dk, sDS, sQ, ID_KV, BN / 16, k > 0);
-                mmas_mm(t_dp, sDS, sK, ID_DQ, BM / 16, 0);
+                mmas_km<BN / 16>(t_dk, sDS, sQ, ID_KV, k > 0);
+                mmas_mm<BM / 16>(t_dp, sDS, sK, ID_DQ, 0);
                 mma_commit(bar(B_DQ_FULL));
                 mma_commit(bar(kStageInQ<D> ? B_DS_FREE : B_Q_EMPTY0 + s));
               }
