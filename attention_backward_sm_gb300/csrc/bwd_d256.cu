@@ -26,8 +26,8 @@
 // through the dO stages once on its way to TMEM), dS 16 KB, dQ staging
 // 16 KB, statistics.
 //
-// Warp roles (512 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 4-11 two softmax warpgroups (32 query columns each;
+// Warp roles (512 threads): warp 0 TMA producer (K, V, Q, statistics),
+// warp 2 TMA producer of dO, warp 1 TMEM allocator and MMA issuer, warps 4-11 two softmax warpgroups (32 query columns each;
 // warpgroup 0 also moves V into TMEM; at the end dV_c / dK_c), warps 12-15
 // dQ write-back (lane = head dimension).  Every wait is bounded.
 #include <cuda.h>
@@ -49,7 +49,7 @@ constexpr int BM = 128;                  // key rows per CTA
 constexpr int BN = 64;                   // query rows per block
 constexpr int kThreads = 512;
 constexpr uint32_t kRegLaunch = 65536 / kThreads;
-constexpr uint32_t kRegOther = 48;
+constexpr uint32_t kRegOther = 56;
 constexpr uint32_t kRegSoftmax = 152;
 constexpr uint32_t kRegDrain = 152;
 static_assert(128 * kRegOther + 256 * kRegSoftmax + 128 * kRegDrain <= 65536, "register budgets exceed the launch");
@@ -93,6 +93,14 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t tile, int t, uint32_t chunk)
 __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int t, uint32_t chunk) {
   return sw128_desc(tile + t * 2048, chunk, 1024);
 }
+
+// The same descriptors stepped by constants: the start address is the
+// descriptor's low 14 bits (addr >> 4) and every step stays inside its tile,
+// so the issuing warp builds a group's descriptors once and adds offsets.
+__device__ __forceinline__ constexpr uint64_t step_k(int t, uint32_t chunk) {
+  return ((t >> 2) * chunk + (t & 3) * 32) >> 4;
+}
+__device__ __forceinline__ constexpr uint64_t step_mn(int t) { return (t * 2048) >> 4; }
 
 __device__ __forceinline__ int floordiv(long long a, int b) {
   long long q = a / b;
@@ -218,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         }
       }
       __syncwarp();
-      int pend_kv = 1, pend_q = -1, pend_do = -1;
-      uint32_t par_q = 0, par_do = 0;
+      int pend_kv = 1, pend_q = -1;
+      uint32_t par_q = 0;
       bool ok = mbar_wait(bar(B_KV_FULL), 0, abort, status);
       if (ok) {
         pend_kv = 0;
@@ -287,14 +295,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
+      }
+      volatile int no_abort = 0;
+      if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
+      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dO producer
+    // (its own warp, so that Q and dO loads are issued independently)
+    setmaxnreg_to<kRegOther, kRegLaunch>();
+    if (n_it > 0) {
+      int pend_do = -1;
+      uint32_t par_do = 0;
+      for (int k = 0; k < n_it; ++k) {
+        const int s = k & 1;
+        const uint32_t prev = ((k >> 1) - 1) & 1;
+        const int qb = qb_of(k);
+        const int q_valid = min(BN, s1 - qb * BN);
         // the dO stages hold V until warpgroup 0 has moved it into TMEM
         if (k == 0 && !mbar_wait(bar(B_V_DONE), 0, abort, status)) break;
         if (k >= 2 && !mbar_wait(bar(B_DO_EMPTY0 + s), prev, abort, status)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_DO_FULL0 + s), TILE_Q);
           for (int ch = 0; ch < 4; ++ch)
-            tma_load_2d(sbase + L::DO + s * TILE_Q + ch * CHUNK_Q, &p.tm_do, hq * D + ch * 64, q_row0,
-                        bar(B_DO_FULL0 + s));
+            tma_load_2d(sbase + L::DO + s * TILE_Q + ch * CHUNK_Q, &p.tm_do, hq_of(k) * D + ch * 64,
+                        q_start + qb * BN, bar(B_DO_FULL0 + s));
         }
         pend_do = s;
         par_do = (k >> 1) & 1;
@@ -308,8 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(bar(B_DO_READY0 + s));
       }
       volatile int no_abort = 0;
-      if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
-      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
       if (pend_do >= 0) mbar_wait(bar(B_DO_FULL0 + pend_do), par_do, &no_abort, status);
     }
   } else if (warp == 1) {
@@ -327,9 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
       if (ok) {
         tc_fence_after();
         if (elect_one()) {
-#pragma unroll 1
+          const uint64_t a0 = desc_k(sK, 0, CHUNK_K), b0 = desc_k(sbase + L::Q, 0, CHUNK_Q);
+#pragma unroll 4
           for (int t = 0; t < D / 16; ++t)
-            mma_ss(t_s, desc_k(sK, t, CHUNK_K), desc_k(sbase + L::Q, t, CHUNK_Q), ID_S, t > 0);
+            mma_ss(t_s, a0 + step_k(t, CHUNK_K), b0 + step_k(t, CHUNK_Q), ID_S, t > 0);
           mma_commit(bar(B_S_FULL));
         }
         __syncwarp();
@@ -344,8 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         if (!mbar_wait(bar(B_DO_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-#pragma unroll 1
-          for (int t = 0; t < D / 16; ++t) mma_ts(t_dp, t_v + t * 8, desc_k(sDO, t, CHUNK_Q), ID_S, t > 0);
+          const uint64_t b0 = desc_k(sDO, 0, CHUNK_Q);
+#pragma unroll 4
+          for (int t = 0; t < D / 16; ++t) mma_ts(t_dp, t_v + t * 8, b0 + step_k(t, CHUNK_Q), ID_S, t > 0);
           mma_commit(bar(B_DP_FULL));
         }
         __syncwarp();
@@ -355,10 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         if (!mbar_wait(bar(B_P_READY), ph, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-#pragma unroll 1
+          const uint64_t b0 = desc_mn(sDO + 2 * c * CHUNK_Q, 0, CHUNK_Q);
+#pragma unroll
           for (int t = 0; t < BN / 16; ++t)
-            mma_ts(t_dv, t_s + (t >> 1) * 32 + (t & 1) * 8, desc_mn(sDO + 2 * c * CHUNK_Q, t, CHUNK_Q), ID_KV,
-                   (k > 0) | (t > 0));
+            mma_ts(t_dv, t_s + (t >> 1) * 32 + (t & 1) * 8, b0 + step_mn(t), ID_KV, (k > 0) | (t > 0));
           mma_commit(bar(B_P_USED));
           mma_commit(bar(B_DO_EMPTY0 + s));
         }
@@ -379,9 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
               tc_fence_after();
               if (elect_one()) {
                 const uint32_t sQn = sbase + L::Q + s1n * TILE_Q;
-#pragma unroll 1
+                const uint64_t a0 = desc_k(sK, 0, CHUNK_K), b0 = desc_k(sQn, 0, CHUNK_Q);
+#pragma unroll 4
                 for (int t = 0; t < D / 16; ++t)
-                  mma_ss(t_s, desc_k(sK, t, CHUNK_K), desc_k(sQn, t, CHUNK_Q), ID_S, t > 0);
+                  mma_ss(t_s, a0 + step_k(t, CHUNK_K), b0 + step_k(t, CHUNK_Q), ID_S, t > 0);
                 mma_commit(bar(B_S_FULL));
               }
               __syncwarp();
@@ -390,14 +416,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
               tc_fence_after();
               if (elect_one()) {
                 // dK_c += dS^T Q_i[:, half c]   (A = dS, K-major over queries)
-#pragma unroll 1
+                const uint64_t a0 = desc_k(sDS, 0, CHUNK_K), b0 = desc_mn(sQ + 2 * c * CHUNK_Q, 0, CHUNK_Q);
+#pragma unroll
                 for (int t = 0; t < BN / 16; ++t)
-                  mma_ss(t_dk, desc_k(sDS, t, CHUNK_K), desc_mn(sQ + 2 * c * CHUNK_Q, t, CHUNK_Q), ID_KV,
-                         (k > 0) | (t > 0));
+                  mma_ss(t_dk, a0 + step_k(t, CHUNK_K), b0 + step_mn(t), ID_KV, (k > 0) | (t > 0));
                 // dQ_c^T = K_c^T dS^T into the dP columns (both MN-major, K = keys)
-#pragma unroll 1
-                for (int t = 0; t < BM / 16; ++t)
-                  mma_ss(t_dp, desc_mn(sKc, t, CHUNK_K), desc_mn(sDS, t, CHUNK_K), ID_DQ, t > 0);
+                const uint64_t a1 = desc_mn(sKc, 0, CHUNK_K), b1 = desc_mn(sDS, 0, CHUNK_K);
+#pragma unroll 4
+                for (int t = 0; t < BM / 16; ++t) mma_ss(t_dp, a1 + step_mn(t), b1 + step_mn(t), ID_DQ, t > 0);
                 mma_commit(bar(B_DQ_FULL));
                 mma_commit(bar(B_Q_EMPTY0 + s));
                 mma_commit(bar(B_DS_FREE));
