@@ -82,6 +82,14 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int t, uint32_t 
   return sw128_desc(tile + t * 2048, chunk, 1024);
 }
 
+// The same descriptors stepped by constants (start address = low 14 bits,
+// addr >> 4; every step stays inside its tile): the issuing thread builds a
+// group's descriptors once and adds offsets.
+__device__ __forceinline__ constexpr uint64_t step_kmajor(int t, uint32_t chunk) {
+  return ((t >> 2) * chunk + (t & 3) * 32) >> 4;
+}
+__device__ __forceinline__ constexpr uint64_t step_mnmajor(int t) { return (t * 2048) >> 4; }
+
 __device__ __forceinline__ int floordiv(long long a, int b) {
   long long q = a / b;
   if ((a % b) != 0 && a < 0) --q;
@@ -217,10 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
-#pragma unroll 1
+        const uint64_t a0 = desc_kmajor(sQ, 0, L::CHUNK_Q), b0 = desc_kmajor(sbase + L::K, 0, L::CHUNK_KV);
+#pragma unroll 4
         for (int t = 0; t < D / 16; ++t)
-          mma_ss(tmem + COL_S0, desc_kmajor(sQ, t, L::CHUNK_Q), desc_kmajor(sbase + L::K, t, L::CHUNK_KV), ID_S,
-                 t > 0);
+          mma_ss(tmem + COL_S0, a0 + step_kmajor(t, L::CHUNK_Q), b0 + step_kmajor(t, L::CHUNK_KV), ID_S, t > 0);
         mma_commit(bar(B_S_FULL0));
       }
       __syncwarp();
@@ -235,9 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         tc_fence_after();
         if (elect_one()) {
           const uint32_t sK = sbase + L::K + s1n * L::TILE_KV;
-#pragma unroll 1
+          const uint64_t a0 = desc_kmajor(sQ, 0, L::CHUNK_Q), b0 = desc_kmajor(sK, 0, L::CHUNK_KV);
+#pragma unroll 4
           for (int t = 0; t < D / 16; ++t)
-            mma_ss(tmem + COL_S0 + s1n * BK, desc_kmajor(sQ, t, L::CHUNK_Q), desc_kmajor(sK, t, L::CHUNK_KV), ID_S,
+            mma_ss(tmem + COL_S0 + s1n * BK, a0 + step_kmajor(t, L::CHUNK_Q), b0 + step_kmajor(t, L::CHUNK_KV), ID_S,
                    t > 0);
           mma_commit(bar(B_S_FULL0 + s1n));
         }
@@ -247,10 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       tc_fence_after();
       if (elect_one()) {
         const uint32_t sV = sbase + L::V + s * L::TILE_KV;
-#pragma unroll 1
+        const uint64_t b0 = desc_mnmajor(sV, 0, L::CHUNK_KV);
+#pragma unroll 4
         for (int t = 0; t < BK / 16; ++t)
-          mma_ts(tmem + L::COL_O, tmem + COL_S0 + s * BK + t * 8, desc_mnmajor(sV, t, L::CHUNK_KV), ID_O,
-                 (j > 0) | (t > 0));
+          mma_ts(tmem + L::COL_O, tmem + COL_S0 + s * BK + t * 8, b0 + step_mnmajor(t), ID_O, (j > 0) | (t > 0));
         mma_commit(bar(B_O_DONE));
         mma_commit(bar(B_KV_EMPTY0 + s));
       }
