@@ -60,27 +60,35 @@ def _check(rc: int):
         raise FabwdError(rc, fa_last_error())
 
 
+# The helpers below run on every call; they are kept to plain attribute
+# reads because small problems are bound by the host time of a launch.
 def _ptr(t) -> int | None:
     if t is None:
         return None
-    return t.data_ptr() if t.numel() > 0 else None
+    return t.data_ptr() or None
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream) -> int | None:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return stream.cuda_stream or None
+    if stream is not None:
+        return stream.cuda_stream or None
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device()) or None
+    return torch.cuda.current_stream().cuda_stream or None
 
 
 def _host_offsets(cu) -> np.ndarray:
+    if isinstance(cu, np.ndarray) and cu.dtype == np.int32 and cu.flags.c_contiguous:
+        return cu
     if isinstance(cu, torch.Tensor):
         cu = cu.detach().cpu().numpy()
-    a = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
-    return a
+    return np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
 
 
-def _hp(a: np.ndarray):
-    return a.ctypes.data_as(ctypes.c_void_p)
+def _hp(a: np.ndarray) -> int:
+    return a.ctypes.data
 
 
 def _shape(q):

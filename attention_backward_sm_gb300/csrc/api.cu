@@ -9,6 +9,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fabwd.h"
@@ -126,14 +127,18 @@ int make_map(CUtensorMap* m, const void* base, int rows, int heads, int head_dim
 }
 
 int check_device() {
+  static std::atomic<unsigned long long> ok_mask{0};   // devices already found to be sm_103
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (ok_mask.load(std::memory_order_acquire) & bit)) return FA_OK;
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (major != 10 || minor != 3)
     return fail(FA_ERR_UNSUPPORTED, "this library is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  if (bit) ok_mask.fetch_or(bit, std::memory_order_release);
   return FA_OK;
 }
 

@@ -690,7 +690,8 @@ cudaError_t launch_bwd256(const BwdParams& p, int batch, int max_kv_blocks, cuda
   if (batch <= 0 || max_kv_blocks <= 0) return cudaSuccess;
   constexpr uint32_t bytes = Layout::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd256_kernel), (int)bytes, smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid(max_kv_blocks, p.heads_kv, 2 * batch);
   bwd256_kernel<<<grid, kThreads, bytes, s>>>(p);

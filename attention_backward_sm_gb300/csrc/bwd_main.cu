@@ -794,7 +794,8 @@ template <int D>
 cudaError_t launch_d(const BwdParams& p, int batch, int max_kv_blocks, cudaStream_t s) {
   constexpr uint32_t bytes = Layout<D>::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D>), (int)bytes, smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid(max_kv_blocks, p.heads_kv, batch);
   bwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);

@@ -435,7 +435,8 @@ template <int D>
 cudaError_t launch_d(const FwdTcParams& p, int batch, int max_q_blocks, cudaStream_t s) {
   constexpr uint32_t bytes = Layout<D>::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fwd_kernel<D>), (int)bytes, smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid(max_q_blocks, p.heads, batch);
   fwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace fa {
 
 // Everything the single-pass backward kernel needs, passed by value as one
@@ -70,6 +72,19 @@ struct FwdTcParams {
 };
 cudaError_t launch_fwd_main(const FwdTcParams& p, int head_dim, int batch, int max_q_blocks, cudaStream_t s);
 int fwd_read_and_clear_status(cudaStream_t s, int* status);
+
+// Sets a kernel's dynamic shared-memory limit once per device (the first
+// call with that device current); `done` is the kernel's per-device mask.
+inline cudaError_t set_smem_once(const void* func, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Records a message for fa_last_error() on the calling thread and returns code.
 int set_last_error(int code, const char* fmt, ...);

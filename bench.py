@@ -318,6 +318,7 @@ def run_gpu(args):
     fab.lib()
 
     case = make_case(args.workload)
+    cu_q_host, cu_kv_host = case.cu_q, case.cu_kv      # host offsets, computed once
     q, k, v, do = (t.to(dev) for t in case_tensors(case))
     cu_q = torch.from_numpy(case.cu_q).to(dev)
     cu_kv = torch.from_numpy(case.cu_kv).to(dev)
@@ -325,12 +326,12 @@ def run_gpu(args):
     mask = fab.mask_kind(case.causal, case.bottom_right)
     lse_stats = args.stats == "lse"
     if lse_stats:
-        o, lse = fab.forward_lse(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, **mask_kw(case))
+        o, lse = fab.forward_lse(q, k, v, cu_q, cu_kv, cu_q_host, cu_kv_host, case.causal, scale, **mask_kw(case))
         stats = (lse,)
     else:
-        o, m, l = fab.forward_stats(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, **mask_kw(case))
+        o, m, l = fab.forward_stats(q, k, v, cu_q, cu_kv, cu_q_host, cu_kv_host, case.causal, scale, **mask_kw(case))
         stats = (m, l)
-    work = fab.Workspace(q, case.cu_q, case.cu_kv, case.causal, args.dq_mode)
+    work = fab.Workspace(q, cu_q_host, cu_kv_host, case.causal, args.dq_mode)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
     flops = useful_flops(case)
@@ -342,10 +343,10 @@ def run_gpu(args):
         if ev is not None:
             ev[0].record(stream)
         if lse_stats:
-            fab.fa_bwd_lse(q, k, v, do, stats[0], work.D, work.dq_acc, dk, dv, cu_q, cu_kv, case.cu_q, case.cu_kv,
+            fab.fa_bwd_lse(q, k, v, do, stats[0], work.D, work.dq_acc, dk, dv, cu_q, cu_kv, cu_q_host, cu_kv_host,
                            mask, case.window, scale, args.dq_mode, work.ws)
         else:
-            fab.fa_bwd_ex(q, k, v, do, *stats, work.D, work.dq_acc, dk, dv, cu_q, cu_kv, case.cu_q, case.cu_kv,
+            fab.fa_bwd_ex(q, k, v, do, *stats, work.D, work.dq_acc, dk, dv, cu_q, cu_kv, cu_q_host, cu_kv_host,
                           mask, case.window, scale, args.dq_mode, work.ws)
         if ev is not None:
             ev[1].record(stream)
@@ -358,6 +359,14 @@ def run_gpu(args):
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Inputs that fit in L2 would stay cached from one step to the next: every
+    # timed step is then preceded by writing a buffer four times the L2, and
+    # timed by its own events.  While that write runs the host enqueues the
+    # whole step, so no host-side gap falls inside the timed interval.
+    small = input_bytes <= L2_BYTES
+    flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=dev) if small else None
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if small else None
     clocks = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     if pg is not None:
@@ -365,14 +374,19 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     start.record(stream)
     for i in range(args.steps):
+        if small:
+            flush.zero_()
+            step_evs[i][0].record(stream)
         step(evs[i])
+        if small:
+            step_evs[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     if pg is not None:
         pg.barrier()
     clk = clocks.stop() if clocks else None
     fab.fa_check_device_status()
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = sum(a.elapsed_time(b) for a, b in step_evs) if small else start.elapsed_time(end)
     bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     elapsed_ms, bwd_ms = max_over_ranks([elapsed_ms, bwd_ms], pg, dev)
     ms_per_step = elapsed_ms / args.steps
@@ -392,7 +406,7 @@ def run_gpu(args):
             for d_, h_ in zip(dev_in, host_in):
                 d_.copy_(h_, non_blocking=True)
             api = fab.backward_lse if lse_stats else fab.backward
-            outs = api(*dev_in, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, scale, args.dq_mode,
+            outs = api(*dev_in, cu_q, cu_kv, cu_q_host, cu_kv_host, case.causal, scale, args.dq_mode,
                        out=(dq, dk, dv), work=work, **mask_kw(case))
             for h_, d_ in zip(host_out, outs):
                 h_.copy_(d_, non_blocking=True)
@@ -436,7 +450,9 @@ def run_gpu(args):
         "config": {"workload": f"{args.workload}: {workload_desc(case)}", "dq_mode": args.dq_mode,
                    "statistics": "lse" if lse_stats else "m, l",
                    "l2": f"inputs larger than L2 ({input_bytes / 2**20:.0f} MiB resident per step)"
-                   if input_bytes > L2_BYTES else "inputs smaller than L2",
+                   if input_bytes > L2_BYTES else
+                   f"L2 flushed before every timed step ({4 * L2_BYTES / 2**20:.0f} MiB written; inputs "
+                   f"{input_bytes / 2**20:.0f} MiB)",
                    "flops_per_step": flops},
         "frac_of_peak_step": value / world / peak,
         "roofline": roofline,
