@@ -307,7 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   const int n_it = G * n_qit;                       // iterations of the sweep
   const int n_kvb = (s2 + BM - 1) / BM;
   const int nq_div = max(1, n_qit);                 // divisor that stays valid when there is no work
-  auto qb_of = [&](int k) { return qb0 + k % nq_div; };
+  // Deterministic dQ without a mask on a square block grid: key block j
+  // starts its sweep at query block j, so a query block receives its key
+  // blocks' partials one step apart (j, j-1, j-2, ... mod n), which is then
+  // the fixed order of the additions; every block is added to just in time
+  // instead of all key blocks queueing on the same query block.
+  const bool rotate = p.dq_mode != 0 && !p.causal && n_qit == n_kvb;
+  const int rot = rotate ? kvb : 0;
+  auto qb_of = [&](int k) { return qb0 + (k % nq_div + rot) % nq_div; };
   auto hq_of = [&](int k) { return hk * G + k / nq_div; };
   const long long rs_kv = static_cast<long long>(p.heads_kv) * D;   // key-side row stride (elements)
 
@@ -737,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const long long q0 = static_cast<long long>(qb) * BN;
         const int kb_hi = p.causal ? min(n_kvb - 1, floordiv(q0 + BN - 1 + off, BM)) : n_kvb - 1;
         const int kb_lo = (p.causal && W > 0) ? max(0, floordiv(q0 + off - W + 1, BM)) : 0;
-        const int before = p.kv_reverse ? kb_hi - kvb : kvb - kb_lo;
+        const int before = rotate ? (qb - kvb + n_kvb) % n_kvb : p.kv_reverse ? kb_hi - kvb : kvb - kb_lo;
         turn = wait_counter(ticket, before, abort, status);
         fence_proxy_async_global();
       }

@@ -123,6 +123,9 @@ def test_single_key_degenerate(d):
 @pytest.mark.parametrize("case", [
     si.fixed("det_d128_causal_tail", 2, 3, 128, 700, 700, True, 51),
     si.Case("det_d64_varlen_cross", 3, 64, [300, 1, 513], [257, 700, 129], False, 52, pad_q=5, pad_kv=3),
+    # square without a mask: key blocks sweep the query blocks in rotated order
+    si.fixed("det_d128_noncausal_square_tail", 2, 3, 128, 700, 700, False, 53),
+    si.fixed("det_d64_noncausal_square", 1, 2, 64, 1024, 1024, False, 54, heads_kv=1),
 ], ids=lambda c: c.name)
 def test_deterministic_mode(case):
     """FA_DQ_DETERMINISTIC: parity with the oracle, and dQ bitwise identical
@@ -143,6 +146,19 @@ def test_deterministic_full_size_cfg3_causal_bitwise():
     import attention_backward_sm_gb300 as fab
     case = si.cfg3(True)
     subset = sampled(case, 2, seed=7)
+    prep = Prepared(case, heads_subset=subset)
+    first = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
+    check_case(prep, out=first)
+    again = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
+    assert torch.equal(first[0], again[0])
+
+
+def test_deterministic_full_size_noncausal_bitwise():
+    """Full-size batch without a mask (rotated sweep order) in deterministic
+    mode: two runs agree bit for bit and the sampled heads match the oracle."""
+    import attention_backward_sm_gb300 as fab
+    case = si.cfg3(False)
+    subset = sampled(case, 2, seed=8)
     prep = Prepared(case, heads_subset=subset)
     first = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
     check_case(prep, out=first)
