@@ -180,7 +180,7 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first, int lane) {
 // a loop without any per-element mask work.  Every mask (tails, causal
 // in either alignment, sliding window) leaves key row r a single run of
 // visible query columns of the tile: [c_lo, c_lo + span) (span <= 0: none).
-// lse4: the 64 per-column lse2 values in shared memory; pre: the first 32
+// lse4: the 64 per-column values -lse2 in shared memory; pre: the first 32
 // of them, read earlier.  The second 32 are read while the first TMEM load
 // is in flight.
 template <bool MASK>
@@ -198,12 +198,17 @@ __device__ __forceinline__ void softmax_p(uint32_t taddr, const float4* lse4, co
     tmem_ld_wait();
 #pragma unroll
     for (int c4 = 0; c4 < 8; ++c4) {
-      const float4 lv = half == 0 ? pre[c4] : nxt[c4];
-      const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+      const float4 lv = half == 0 ? pre[c4] : nxt[c4];   // -lse2 of 4 columns
+      // exponent arguments two at a time (packed fp32 FMA)
+      const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(v[c4 * 4]), __uint_as_float(v[c4 * 4 + 1])),
+                                    make_float2(sl2, sl2), make_float2(lv.x, lv.y));
+      const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(v[c4 * 4 + 2]), __uint_as_float(v[c4 * 4 + 3])),
+                                    make_float2(sl2, sl2), make_float2(lv.z, lv.w));
+      const float xs[4] = {x01.x, x01.y, x23.x, x23.y};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int col = half * 32 + c4 * 4 + e;
-        float pv = ex2_approx(fmaf(__uint_as_float(v[c4 * 4 + e]), sl2, -la[e]));
+        float pv = ex2_approx(xs[e]);
         if (MASK) {
           const bool vis = static_cast<unsigned>(qc0 + col - c_lo) < static_cast<unsigned>(span);
           pv = vis ? pv : 0.f;
@@ -221,7 +226,7 @@ __device__ __forceinline__ void softmax_p(uint32_t taddr, const float4* lse4, co
 
 // dS phase of one softmax thread: dS = P * (dP - D) from dP^T in TMEM,
 // rounded to bf16 and written as row r of the 128B-swizzled dS tile.
-// dvec4: the 64 per-column D values in shared memory; pre: the first 32.
+// dvec4: the 64 per-column values -D in shared memory; pre: the first 32.
 template <bool MASK>
 __device__ __forceinline__ void softmax_ds(uint32_t taddr, const float4* dvec4, const float4 (&pre)[8],
                                            const float (&P)[64], uint32_t ds_row, int r) {
@@ -238,15 +243,20 @@ __device__ __forceinline__ void softmax_ds(uint32_t taddr, const float4* dvec4, 
     uint32_t pk[16];
 #pragma unroll
     for (int c4 = 0; c4 < 8; ++c4) {
-      const float4 dv4 = half == 0 ? pre[c4] : nxt[c4];
-      const float da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-      float ds[4];
+      const float4 dv4 = half == 0 ? pre[c4] : nxt[c4];   // -D of 4 columns
+      const int c0 = half * 32 + c4 * 4;
+      // dS = P * (dP - D), two at a time (packed fp32 add and multiply)
+      const float2 d01 = __fmul2_rn(make_float2(P[c0], P[c0 + 1]),
+                                    __fadd2_rn(make_float2(__uint_as_float(v[c4 * 4]), __uint_as_float(v[c4 * 4 + 1])),
+                                               make_float2(dv4.x, dv4.y)));
+      const float2 d23 = __fmul2_rn(make_float2(P[c0 + 2], P[c0 + 3]),
+                                    __fadd2_rn(make_float2(__uint_as_float(v[c4 * 4 + 2]), __uint_as_float(v[c4 * 4 + 3])),
+                                               make_float2(dv4.z, dv4.w)));
+      float ds[4] = {d01.x, d01.y, d23.x, d23.y};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int c = half * 32 + c4 * 4 + e;
-        ds[e] = P[c] * (__uint_as_float(v[c4 * 4 + e]) - da[e]);
         // P is already 0 where masked, but dP may hold garbage there.
-        if (MASK) ds[e] = (P[c] != 0.f) ? ds[e] : 0.f;
+        if (MASK) ds[e] = (P[c0 + e] != 0.f) ? ds[e] : 0.f;
       }
       pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
       pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
@@ -440,8 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           // log2 of the softmax denominator, exp(x - m) / l = 2^(x*log2e - lse2)
-          st_lse[s * 128 + lane + 32 * j] = rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j]));
-          st_D[s * 128 + lane + 32 * j] = rd[j];
+          // stored negated: the softmax adds them with packed FMAs / adds
+          st_lse[s * 128 + lane + 32 * j] = -(rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j])));
+          st_D[s * 128 + lane + 32 * j] = -rd[j];
         }
         if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;
         pend_q = -1;
