@@ -101,3 +101,62 @@ def test_gqa_host_argument_checks(lib):
     # shape checks still come first
     assert lib.fa_bwd_gqa(p, p, p, p, p, p, p, p, p, p, p, p, hp, hp, 2, 30, 30, 4, 2, 96, 0, 0.1, 0,
                           None, 0, None) == 2
+
+
+def _call_bwd_ex(lib, cu_q, cu_kv, mask=1, window=0, heads=2, heads_kv=2, head_dim=128, dq_mode=0):
+    p = ctypes.c_void_p(16)
+    hq, hk = cu_q.ctypes.data_as(ctypes.c_void_p), cu_kv.ctypes.data_as(ctypes.c_void_p)
+    return lib.fa_bwd_ex(p, p, p, p, p, p, p, p, p, p, p, p, hq, hk, len(cu_q) - 1, int(cu_q[-1]), int(cu_kv[-1]),
+                         heads, heads_kv, head_dim, mask, window, 0.1, dq_mode, None, 0, None)
+
+
+def test_mask_and_window_argument_checks(lib):
+    """fa_bwd_ex / fa_fwd_stats_ex reject unknown masks, negative windows and
+    a window without a causal mask before touching the device."""
+    cu = _offsets(0, 10, 30)
+    assert _call_bwd_ex(lib, cu, cu, mask=3) == 1
+    assert b"mask" in lib.fa_last_error()
+    assert _call_bwd_ex(lib, cu, cu, mask=-1) == 1
+    assert _call_bwd_ex(lib, cu, cu, mask=1, window=-5) == 1
+    assert b"window" in lib.fa_last_error()
+    assert _call_bwd_ex(lib, cu, cu, mask=0, window=4) == 1
+    assert b"causal" in lib.fa_last_error()
+    p = ctypes.c_void_p(16)
+    hp = cu.ctypes.data_as(ctypes.c_void_p)
+    assert lib.fa_fwd_stats_ex(p, p, p, p, p, p, p, p, hp, hp, 2, 30, 30, 2, 2, 128, 0, 7, 0.1, None) == 1
+    assert lib.fa_fwd_lse(p, p, p, p, p, p, p, hp, hp, 2, 30, 30, 2, 2, 128, 5, 0, 0.1, None) == 1
+    # the plain entry points keep accepting only a 0/1 causal flag
+    assert _call_bwd(lib, cu, cu, causal=2) == 1
+
+
+def test_head_dim_256_is_accepted_and_others_are_not(lib):
+    cu = _offsets(0, 10, 30)
+    # head_dim 256 passes the shape checks (then stops at a NULL device pointer, not UNSUPPORTED)
+    p = ctypes.c_void_p(16)
+    hp = cu.ctypes.data_as(ctypes.c_void_p)
+    rc = lib.fa_bwd_ex(None, None, None, None, None, None, None, None, None, None, None, None, hp, hp, 2, 30, 30,
+                       2, 2, 256, 1, 0, 0.1, 0, None, 0, None)
+    assert rc == 1 and b"NULL" in lib.fa_last_error()
+    for d in (32, 96, 192, 512):
+        assert _call_bwd_ex(lib, cu, cu, head_dim=d) == 2
+        assert b"head_dim" in lib.fa_last_error()
+    assert lib.fa_bwd_preprocess(p, p, p, p, 10, 2, 192, None) == 2
+
+
+def test_workspace_size_head_dim_256(lib):
+    """Deterministic mode at head_dim 256 counts 64-row query blocks, two
+    head-dim halves and four 32-dim quarters per (batch, head)."""
+    cu = _offsets(0, 300, 700)
+    hp = cu.ctypes.data_as(ctypes.c_void_p)
+    n = lib.fa_bwd_workspace_size(hp, hp, 2, 4, 256, 0, 1)
+    assert n >= 2 * 4 * 7 * 8 * 4 and n % 256 == 0            # max_q = 400 -> 7 blocks of 64
+    assert lib.fa_bwd_workspace_size(hp, hp, 2, 4, 256, 0, 0) == 0
+
+
+def test_lse_entry_points_need_no_l(lib):
+    """fa_bwd_lse has no l argument: with no work it succeeds, and its
+    pointer checks do not ask for one."""
+    z = _offsets(0)
+    hp = z.ctypes.data_as(ctypes.c_void_p)
+    assert lib.fa_bwd_lse(None, None, None, None, None, None, None, None, None, None, None, hp, hp, 0, 0, 0,
+                          2, 2, 128, 1, 0, 0.1, 0, None, 0, None) == 0
