@@ -223,6 +223,12 @@ def fa_bwd_noalloc(q, k, v, o, do, m, l, dq, dk, dv, cu_q_dev, cu_kv_dev, cu_q_h
                                 total_kv, heads, dim, int(bool(causal)), float(scale), _stream(stream)))
 
 
+def fa_selftest_wait_timeout(stream=None):
+    """Launches a block whose bounded wait runs out (about 4 s); the next
+    fa_check_device_status raises FabwdError with FA_ERR_TIMEOUT."""
+    _check(lib().fa_selftest_wait_timeout(_stream(stream)))
+
+
 def fa_check_device_status(stream=None):
     _check(lib().fa_check_device_status(_stream(stream)))
 

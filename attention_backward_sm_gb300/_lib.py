@@ -34,6 +34,7 @@ SIGNATURES = {
     "fa_bwd_dq_finalize": (_i, [_p, _p, _i, _i, _i, _f, _p]),
     "fa_bwd_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                             _i, _i, _i, _i, _i, _i, _f, _p]),
+    "fa_selftest_wait_timeout": (_i, [_p]),
     "fa_check_device_status": (_i, [_p]),
     "fa_last_error": (ctypes.c_char_p, []),
 }

@@ -440,6 +440,14 @@ int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads,
   return ok();
 }
 
+int fa_selftest_wait_timeout(fa_stream_t stream) {
+  int rc = check_device();
+  if (rc) return rc;
+  cudaError_t e = fa::launch_wait_timeout(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ok();
+}
+
 int fa_check_device_status(fa_stream_t stream) {
   int st = 0, st256 = 0, st_fwd = 0;
   int e = fa::bwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st);

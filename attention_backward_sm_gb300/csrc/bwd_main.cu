@@ -827,6 +827,30 @@ cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max
   return head_dim == 64 ? launch_d<64>(p, batch, max_kv_blocks, s) : launch_d<128>(p, batch, max_kv_blocks, s);
 }
 
+namespace {
+
+// Waits, through the kernels' own bounded mbarrier wait, on a barrier that
+// nothing arrives on: the wait gives up after its time limit and records the
+// timeout code in the status word, and the kernel returns normally.
+__global__ void wait_timeout_kernel() {
+  __shared__ __align__(8) uint64_t never;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&never), 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&never), 0, &abort_flag, &g_bwd_status);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout(cudaStream_t s) {
+  wait_timeout_kernel<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
+
 int bwd_read_and_clear_status(cudaStream_t s, int* status) {
   int zero = 0;
   cudaError_t e = cudaStreamSynchronize(s);

@@ -46,6 +46,7 @@ cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max
 cudaError_t launch_bwd256(const BwdParams& p, int batch, int max_kv_blocks, cudaStream_t s);
 int bwd256_read_and_clear_status(cudaStream_t s, int* status);
 int bwd_read_and_clear_status(cudaStream_t s, int* status);
+cudaError_t launch_wait_timeout(cudaStream_t s);
 
 cudaError_t launch_preprocess(const uint16_t* o, const uint16_t* dout, float* D, float* dq_acc, long long rows,
                               int head_dim, cudaStream_t s);

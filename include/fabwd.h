@@ -253,6 +253,15 @@ int fa_bwd_noalloc(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const f
                    int batch, int total_q, int total_kv, int heads, int head_dim,
                    int causal, float scale, fa_stream_t stream);
 
+/* Diagnostic (the pages have no counterpart): launches one block that
+ * waits, through the same bounded mbarrier wait the kernels use, on a
+ * barrier nothing arrives on.  After the wait's time limit (4 s) it records
+ * FA_ERR_TIMEOUT in the device status word and returns; nothing faults and
+ * the context stays usable.  The next fa_check_device_status on `stream`
+ * then returns FA_ERR_TIMEOUT.  Lets a caller test its handling of a timed
+ * out kernel. */
+int fa_selftest_wait_timeout(fa_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device status word
  * that bounded waits set.  Returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_CUDA. */
 int fa_check_device_status(fa_stream_t stream);

@@ -71,3 +71,24 @@ def test_unsupported_head_dim_raises():
 def test_device_status_clean_after_runs():
     import attention_backward_sm_gb300 as fab
     fab.fa_check_device_status()
+
+
+def test_bounded_wait_times_out_into_a_status_code():
+    """A wait that nothing satisfies ends after its limit with FA_ERR_TIMEOUT
+    in the status word (no trap, no hang), and the context stays usable: a
+    backward right after runs and reports a clean status."""
+    import attention_backward_sm_gb300 as fab
+    fab.fa_check_device_status()
+    fab.fa_selftest_wait_timeout()
+    with pytest.raises(fab.FabwdError) as e:
+        fab.fa_check_device_status()
+    assert e.value.code == fab.FA_ERR_TIMEOUT
+    fab.fa_check_device_status()                # the word was cleared
+    case = si.fixed("after_timeout", 1, 2, 128, 200, 200, True, 43)
+    q, k, v, do = (t.cuda() for t in case.tensors())
+    cu = torch.from_numpy(case.cu_q).cuda()
+    o, m, l = fab.forward_stats(q, k, v, cu, cu, case.cu_q, case.cu_kv, True, case.softmax_scale)
+    dq, dk, dv = fab.backward(q, k, v, o, do, m, l, cu, cu, case.cu_q, case.cu_kv, True, case.softmax_scale)
+    torch.cuda.synchronize()
+    fab.fa_check_device_status()
+    assert torch.isfinite(dq.float()).all() and torch.isfinite(dk.float()).all()
