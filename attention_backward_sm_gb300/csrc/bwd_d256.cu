@@ -132,16 +132,38 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first, int rows, ui
   }
 }
 
+template <bool kChunked>
 __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                               : static_cast<int>(blockIdx.x);
-  const int hk = blockIdx.y;
-  const int b = blockIdx.z >> 1, c = blockIdx.z & 1;      // c: head-dimension half
+  // Launch order as in the 64/128 kernel.  head_chunk = 1: grid (key block,
+  // key/value head, 2 x sequence + head-dimension half).  head_chunk > 1:
+  // (sequence, key/value head) units in chunks, key block slow within a
+  // chunk, the two head-dimension halves of a key block side by side.
+  int kvb, hk, b, c;                                 // c: head-dimension half
+  if constexpr (!kChunked) {
+    kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                       : static_cast<int>(blockIdx.x);
+    hk = blockIdx.y;
+    b = blockIdx.z >> 1;
+    c = blockIdx.z & 1;
+  } else {
+    const int lin = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+    const int units = p.heads_kv * p.batch;
+    const int per_chunk = p.head_chunk * 2 * p.grid_kv;
+    const int ch = lin / per_chunk;
+    const int r = lin - ch * per_chunk;
+    const int g = min(p.head_chunk, units - ch * p.head_chunk);
+    const int x = r / g;
+    const int unit = ch * p.head_chunk + (r - x * g);
+    c = x & 1;
+    kvb = x >> 1;
+    hk = unit % p.heads_kv;
+    b = unit / p.heads_kv;
+  }
   const int H = p.heads;
   const int G = p.heads / p.heads_kv;
   const int q_start = p.cu_q[b], s1 = p.cu_q[b + 1] - q_start;
@@ -690,11 +712,20 @@ cudaError_t launch_bwd256(const BwdParams& p, int batch, int max_kv_blocks, cuda
   if (batch <= 0 || max_kv_blocks <= 0) return cudaSuccess;
   constexpr uint32_t bytes = Layout::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
-  static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd256_kernel), (int)bytes, smem_set);
+  static std::atomic<unsigned long long> smem_set{0}, smem_set_chunked{0};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd256_kernel<false>), (int)bytes, smem_set);
+  if (e == cudaSuccess) e = set_smem_once(reinterpret_cast<const void*>(bwd256_kernel<true>), (int)bytes, smem_set_chunked);
   if (e != cudaSuccess) return e;
+  if (2LL * max_kv_blocks * p.heads_kv * batch > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  BwdParams q = p;
+  q.batch = batch;
+  q.grid_kv = max_kv_blocks;
+  q.head_chunk = launch_head_chunk(p, batch, max_kv_blocks, BM, BN, D);
   dim3 grid(max_kv_blocks, p.heads_kv, 2 * batch);
-  bwd256_kernel<<<grid, kThreads, bytes, s>>>(p);
+  if (q.head_chunk > 1)
+    bwd256_kernel<true><<<grid, kThreads, bytes, s>>>(q);
+  else
+    bwd256_kernel<false><<<grid, kThreads, bytes, s>>>(q);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "sm103.cuh"
 
@@ -276,7 +278,7 @@ __device__ __forceinline__ int floordiv(long long a, int b) {
   return static_cast<int>(q);
 }
 
-template <int D>
+template <int D, bool kChunked>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -284,15 +286,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Launch order.  Unchunked (head_chunk = 1): the grid is (key block,
+  // key/value head, sequence), key block fastest.  Chunked: the linear block
+  // index takes the (sequence, key/value head) units in chunks of head_chunk
+  // with the key block as the slow index within a chunk, so under a causal
+  // mask the long sweeps of the low key blocks start first and the short ones
+  // fill the tail, while the chunk's query-side data stays in L2.
   // Deterministic causal runs add dQ partials in descending key-block order
-  // and launch key blocks high to low, so that every CTA a CTA waits for was
-  // launched before it (see the dQ write-back).
-  const int kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                               : static_cast<int>(blockIdx.x);
+  // and launch key blocks high to low (head_chunk = 1), so that every CTA a
+  // CTA waits for was launched before it (see the dQ write-back).
+  int kvb, hk, b;
+  if constexpr (!kChunked) {
+    kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                       : static_cast<int>(blockIdx.x);
+    hk = blockIdx.y;
+    b = blockIdx.z;
+  } else {
+    const int lin = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+    const int units = p.heads_kv * p.batch;
+    const int per_chunk = p.head_chunk * p.grid_kv;
+    const int ch = lin / per_chunk;
+    const int r = lin - ch * per_chunk;
+    const int g = min(p.head_chunk, units - ch * p.head_chunk);
+    const int x = r / g;
+    const int unit = ch * p.head_chunk + (r - x * g);
+    kvb = x;
+    hk = unit % p.heads_kv;
+    b = unit / p.heads_kv;
+  }
   // Grouped-query attention: the CTA owns key/value head hk, shared by the
   // G query heads hk*G .. hk*G+G-1, and sweeps the query blocks of each of
   // them in turn; dK and dV accumulate over the whole group in TMEM.
-  const int hk = blockIdx.y, b = blockIdx.z;
   const int H = p.heads;                            // query heads
   const int G = p.heads / p.heads_kv;
   const int q_start = p.cu_q[b], s1 = p.cu_q[b + 1] - q_start;
@@ -812,15 +836,54 @@ template <int D>
 cudaError_t launch_d(const BwdParams& p, int batch, int max_kv_blocks, cudaStream_t s) {
   constexpr uint32_t bytes = Layout<D>::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
-  static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D>), (int)bytes, smem_set);
+  static std::atomic<unsigned long long> smem_set{0}, smem_set_chunked{0};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D, false>), (int)bytes, smem_set);
+  if (e == cudaSuccess) e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D, true>), (int)bytes, smem_set_chunked);
   if (e != cudaSuccess) return e;
+  if (static_cast<long long>(max_kv_blocks) * p.heads_kv * batch > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  BwdParams q = p;
+  q.batch = batch;
+  q.grid_kv = max_kv_blocks;
+  q.head_chunk = launch_head_chunk(p, batch, max_kv_blocks, BM, BN, D);
   dim3 grid(max_kv_blocks, p.heads_kv, batch);
-  bwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);
+  if (q.head_chunk > 1)
+    bwd_kernel<D, true><<<grid, kThreads, bytes, s>>>(q);
+  else
+    bwd_kernel<D, false><<<grid, kThreads, bytes, s>>>(q);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+// Whether the key blocks' query sweeps differ enough in length for the
+// launch order to matter: the longest sweep against the mean, for the
+// longest sequence (lengths rounded up to whole blocks) and the mask's band.
+static bool causal_sweeps_uneven(const BwdParams& p, int n_kvb, int bm, int bn) {
+  const long long s1 = static_cast<long long>(p.max_q_blocks) * bn, s2 = static_cast<long long>(n_kvb) * bm;
+  const long long off = p.bottom_right ? s2 - s1 : 0;
+  auto fdiv = [](long long a, long long b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
+  long long total = 0, longest = 0;
+  for (long long kvb = 0; kvb < n_kvb; ++kvb) {
+    const long long lo = std::max(0LL, fdiv(kvb * bm - off, bn));
+    const long long hi = p.window > 0 ? std::min<long long>(p.max_q_blocks - 1, fdiv(kvb * bm + bm - 2 - off + p.window, bn))
+                                      : p.max_q_blocks - 1;
+    const long long n = std::max(0LL, hi - lo + 1);
+    total += n;
+    longest = std::max(longest, n);
+  }
+  return 2 * longest * n_kvb > 3 * total;   // longest > 1.5 x mean
+}
+
+int launch_head_chunk(const BwdParams& p, int batch, int n_kvb, int bm, int bn, int head_dim) {
+  // Key blocks fast (chunk 1) unless a causal mask makes the sweeps uneven
+  // and dQ is reduced in any order; then heavy-first, in chunks whose
+  // query-side bytes (Q, dO in bf16 and the fp32 dQ accumulator of one
+  // query head per unit) take about a quarter of L2.
+  constexpr long long kChunkBytes = 32ll << 20;
+  if (!p.causal || p.dq_mode != 0 || !causal_sweeps_uneven(p, n_kvb, bm, bn)) return 1;
+  const long long unit_bytes = static_cast<long long>(p.max_q_blocks) * bn * head_dim * 8;
+  return static_cast<int>(std::max(1LL, std::min<long long>(static_cast<long long>(p.heads_kv) * batch, kChunkBytes / unit_bytes)));
+}
 
 cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, cudaStream_t s) {
   if (batch <= 0 || max_kv_blocks <= 0) return cudaSuccess;

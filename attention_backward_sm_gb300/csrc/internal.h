@@ -36,12 +36,18 @@ struct BwdParams {
   int stats_lse;       // 1: m holds lse = m + ln(l) per row and l is unused
   int dq_mode;
   int max_q_blocks;    // query blocks of the longest query sequence
-  int kv_reverse;      // 1: blockIdx.x counts key blocks from the last one down
+  int kv_reverse;      // 1: key blocks are launched from the last one down
+  int batch;           // sequences
+  int grid_kv;         // key blocks of the longest key sequence (launched per head)
+  int head_chunk;      // (sequence, key/value head) units per launch-order chunk
   float scale;         // softmax scale (multiplies dK in the epilogue)
   float scale_log2;    // scale * log2(e)
 };
 
 cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, cudaStream_t s);
+// (sequence, key/value head) units per launch-order chunk of a backward grid
+// with n_kvb key blocks of bm rows and query blocks of bn rows.
+int launch_head_chunk(const BwdParams& p, int batch, int n_kvb, int bm, int bn, int head_dim);
 // head_dim 256 (bwd_d256.cu): tm_q / tm_do with 64-row boxes, max_q_blocks in 64-row blocks
 cudaError_t launch_bwd256(const BwdParams& p, int batch, int max_kv_blocks, cudaStream_t s);
 int bwd256_read_and_clear_status(cudaStream_t s, int* status);

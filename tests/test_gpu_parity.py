@@ -179,3 +179,27 @@ def test_deterministic_full_size_cross_bitwise():
     again = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
     for a, b in zip(first, again):
         assert torch.equal(a, b)
+
+
+# Causal grids whose key blocks have sweeps of very different lengths launch
+# heavy-first in chunks of (sequence, key/value head) units: 32 MiB of
+# query-side data (Q, dO in bf16 and fp32 dQ per query head) per chunk.
+# These shapes leave a short last chunk; the checked heads include its units.
+CHUNKED = [
+    # 8 MiB per unit -> chunks of 4 units: {4, 1}
+    (fixed("chunk_d128_b1_h5_s8192_causal", 1, 5, 128, 8192, 8192, True, 31), [(0, 0), (0, 3), (0, 4)]),
+    # d = 64, 16384 rows: 8 MiB per unit -> {4, 1}
+    (fixed("chunk_d64_b1_h5_s16384_causal", 1, 5, 64, 16384, 16384, True, 32), [(0, 1), (0, 4)]),
+    # grouped (2 query heads per key/value head), 16 MiB per unit -> {2, 1}
+    (fixed("chunk_gqa_b1_h6_hkv3_s16384_causal", 1, 6, 128, 16384, 16384, True, 33, heads_kv=3),
+     [(0, 4), (0, 5)]),
+    # head_dim 256 (64-row query blocks), 16 MiB per unit -> {2, 1}
+    (fixed("chunk_d256_b1_h3_s8192_causal", 1, 3, 256, 8192, 8192, True, 34), [(0, 0), (0, 2)]),
+    # bottom-right diagonal with s2 slightly above s1: sweeps still uneven; 6 units, one chunk
+    (fixed("chunk_br_b2_h3_s4096_4608", 2, 3, 128, 4096, 4608, True, 35, bottom_right=True), [(0, 2), (1, 0)]),
+]
+
+
+@pytest.mark.parametrize("case,subset", CHUNKED, ids=lambda x: getattr(x, "name", "units"))
+def test_chunked_launch_order_sampled(case, subset):
+    check_case(Prepared(case, heads_subset=subset))
