@@ -205,6 +205,7 @@ int fwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, fa_bf16* o, f
   p.bottom_right = mask == FA_MASK_CAUSAL_BOTTOM_RIGHT;
   p.window = effective_window(window, max_q, max_kv);
   p.stats_lse = stats_lse;
+  p.max_kv = max_kv;
   p.scale = scale;
   cudaError_t e = fa::launch_fwd_main(p, head_dim, batch, (max_q + 127) / 128, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");

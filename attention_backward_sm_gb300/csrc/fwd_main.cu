@@ -31,6 +31,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "sm103.cuh"
 
@@ -103,7 +105,35 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
   asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int D>
+// Launch order of a forward grid (x: query tiles, or pairs of tiles; y: query
+// head; z: sequence).  Under a causal mask later tiles see more keys and go
+// first.  Chunked: the linear block index takes the (sequence, query head)
+// units in chunks of head_chunk with the tile as the slow index within a
+// chunk, so the long tiles of every unit of a chunk start before the short
+// ones and the short ones fill the tail.
+template <bool kChunked>
+__device__ __forceinline__ void fwd_block_of(const FwdTcParams& p, int& x, int& h, int& b) {
+  if constexpr (!kChunked) {
+    x = p.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    h = blockIdx.y;
+    b = blockIdx.z;
+  } else {
+    const int nx = static_cast<int>(gridDim.x);
+    const int lin = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+    const int units = p.heads * p.batch;
+    const int per_chunk = p.head_chunk * nx;
+    const int ch = lin / per_chunk;
+    const int r = lin - ch * per_chunk;
+    const int g = min(p.head_chunk, units - ch * p.head_chunk);
+    const int t = r / g;
+    const int unit = ch * p.head_chunk + (r - t * g);
+    x = nx - 1 - t;   // chunked only under a causal mask
+    h = unit % p.heads;
+    b = unit / p.heads;
+  }
+}
+
+template <int D, bool kChunked>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdTcParams p) {
   using L = Layout<D>;
   constexpr int BK = L::BK;
@@ -112,10 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Under a causal mask later query blocks see more keys: they go first.
-  const int qb = p.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                          : static_cast<int>(blockIdx.x);
-  const int h = blockIdx.y, b = blockIdx.z;
+  int qb, h, b;
+  fwd_block_of<kChunked>(p, qb, h, b);
   const int H = p.heads;
   const int hk = h / (H / p.heads_kv);
   const int q_start = p.cu_q[b], s1 = p.cu_q[b + 1] - q_start;
@@ -469,7 +497,7 @@ struct Layout2 {
   static_assert(COL_O + 2 * D <= TMEM_COLS, "tensor memory budget");
 };
 
-template <int D>
+template <int D, bool kChunked>
 __global__ void __launch_bounds__(kThreads2, 1) fwd2_kernel(const __grid_constant__ FwdTcParams p) {
   using L = Layout2<D>;
   constexpr int BK = L::BK;
@@ -479,9 +507,8 @@ __global__ void __launch_bounds__(kThreads2, 1) fwd2_kernel(const __grid_constan
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int qp = p.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                          : static_cast<int>(blockIdx.x);   // pair of 128-row tiles
-  const int h = blockIdx.y, b = blockIdx.z;
+  int qp, h, b;                                       // qp: pair of 128-row tiles
+  fwd_block_of<kChunked>(p, qp, h, b);
   const int H = p.heads;
   const int hk = h / (H / p.heads_kv);
   const int q_start = p.cu_q[b], s1 = p.cu_q[b + 1] - q_start;
@@ -791,15 +818,51 @@ __global__ void __launch_bounds__(kThreads2, 1) fwd2_kernel(const __grid_constan
   }
 }
 
+// Chunk of the launch order: 1 (tile fastest) unless a causal mask makes
+// the tiles' key ranges differ enough (longest > 1.5 x mean, for the longest
+// sequences, lengths rounded up to whole tiles) for the order to matter;
+// then chunks whose key-side bytes (K and V in bf16, shared by the query
+// heads of a group) take about a quarter of L2.
+int fwd_head_chunk(const FwdTcParams& p, int batch, int n_x, int rows, int bk, int head_dim) {
+  constexpr long long kChunkBytes = 32ll << 20;
+  if (!p.causal || n_x <= 1 || p.max_kv <= 0) return 1;
+  const long long s1 = static_cast<long long>(n_x) * rows, s2 = p.max_kv;
+  const long long off = p.bottom_right ? s2 - s1 : 0;
+  const long long n_kb = (s2 + bk - 1) / bk;
+  auto fdiv = [](long long a, long long b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
+  long long total = 0, longest = 0;
+  for (long long x = 0; x < n_x; ++x) {
+    const long long q0 = x * rows;
+    const long long kb1 = std::min(n_kb - 1, fdiv(q0 + rows - 1 + off, bk));
+    const long long kb0 = p.window > 0 ? std::max(0LL, fdiv(q0 + off - p.window + 1, bk)) : 0;
+    const long long n = std::max(0LL, kb1 - kb0 + 1);
+    total += n;
+    longest = std::max(longest, n);
+  }
+  if (2 * longest * n_x <= 3 * total) return 1;
+  const long long unit_bytes =
+      std::max(1LL, s2 * head_dim * 4 / std::max(1, p.heads / std::max(1, p.heads_kv)));
+  return static_cast<int>(std::max(1LL, std::min<long long>(static_cast<long long>(p.heads) * batch, kChunkBytes / unit_bytes)));
+}
+
 template <int D>
 cudaError_t launch_d2(const FwdTcParams& p, int batch, int max_q_blocks, cudaStream_t s) {
   constexpr uint32_t bytes = Layout2<D>::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
-  static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fwd2_kernel<D>), (int)bytes, smem_set);
+  static std::atomic<unsigned long long> smem_set{0}, smem_set_chunked{0};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fwd2_kernel<D, false>), (int)bytes, smem_set);
+  if (e == cudaSuccess) e = set_smem_once(reinterpret_cast<const void*>(fwd2_kernel<D, true>), (int)bytes, smem_set_chunked);
   if (e != cudaSuccess) return e;
-  dim3 grid((max_q_blocks + 1) / 2, p.heads, batch);   // pairs of 128-row tiles
-  fwd2_kernel<D><<<grid, kThreads2, bytes, s>>>(p);
+  const int n_x = (max_q_blocks + 1) / 2;                // pairs of 128-row tiles
+  if (static_cast<long long>(n_x) * p.heads * batch > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  FwdTcParams q = p;
+  q.batch = batch;
+  q.head_chunk = fwd_head_chunk(p, batch, n_x, 2 * BQ, Layout2<D>::BK, D);
+  dim3 grid(n_x, p.heads, batch);
+  if (q.head_chunk > 1)
+    fwd2_kernel<D, true><<<grid, kThreads2, bytes, s>>>(q);
+  else
+    fwd2_kernel<D, false><<<grid, kThreads2, bytes, s>>>(q);
   return cudaGetLastError();
 }
 
@@ -807,11 +870,19 @@ template <int D>
 cudaError_t launch_d(const FwdTcParams& p, int batch, int max_q_blocks, cudaStream_t s) {
   constexpr uint32_t bytes = Layout<D>::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
-  static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fwd_kernel<D>), (int)bytes, smem_set);
+  static std::atomic<unsigned long long> smem_set{0}, smem_set_chunked{0};
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fwd_kernel<D, false>), (int)bytes, smem_set);
+  if (e == cudaSuccess) e = set_smem_once(reinterpret_cast<const void*>(fwd_kernel<D, true>), (int)bytes, smem_set_chunked);
   if (e != cudaSuccess) return e;
+  if (static_cast<long long>(max_q_blocks) * p.heads * batch > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  FwdTcParams q = p;
+  q.batch = batch;
+  q.head_chunk = fwd_head_chunk(p, batch, max_q_blocks, BQ, Layout<D>::BK, D);
   dim3 grid(max_q_blocks, p.heads, batch);
-  fwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);
+  if (q.head_chunk > 1)
+    fwd_kernel<D, true><<<grid, kThreads, bytes, s>>>(q);
+  else
+    fwd_kernel<D, false><<<grid, kThreads, bytes, s>>>(q);
   return cudaGetLastError();
 }
 

@@ -75,6 +75,9 @@ struct FwdTcParams {
   int bottom_right;
   int window;
   int stats_lse;
+  int max_kv;          // longest key sequence (used on the host for the launch order)
+  int batch;           // sequences
+  int head_chunk;      // (sequence, query head) units per launch-order chunk
   float scale;
 };
 cudaError_t launch_fwd_main(const FwdTcParams& p, int head_dim, int batch, int max_q_blocks, cudaStream_t s);

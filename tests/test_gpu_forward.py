@@ -65,3 +65,29 @@ def test_forward_running_max_moves(grow):
     ramp = torch.linspace(0.2, 3.0, k.shape[0]) if grow else torch.linspace(3.0, 0.2, k.shape[0])
     k = (k.float() * ramp[:, None, None]).to(torch.bfloat16)
     check_forward(case, q, k, v)
+
+
+# Causal grids whose tiles see very different numbers of keys launch in
+# chunks of (sequence, query head) units, longest tiles first; these shapes
+# leave a short last chunk (32 MiB of K and V per chunk), whose heads are
+# among the checked ones.
+CHUNKED = [
+    (si.fixed("fwd_chunk_d128_b1_h20_s8192_causal", 1, 20, 128, 8192, 8192, True, 211), [(0, 0), (0, 19)]),
+    (si.fixed("fwd_chunk_d64_b1_h20_s16384_causal", 1, 20, 64, 16384, 16384, True, 212), [(0, 17)]),
+    (si.fixed("fwd_chunk_d256_b1_h6_s8192_causal", 1, 6, 256, 8192, 8192, True, 213), [(0, 1), (0, 5)]),
+    (si.fixed("fwd_chunk_gqa_b2_h12_hkv3_s4096_causal", 2, 12, 128, 4096, 4096, True, 214, heads_kv=3),
+     [(0, 11), (1, 4)]),
+]
+
+
+@pytest.mark.parametrize("case,subset", CHUNKED, ids=lambda x: getattr(x, "name", "heads"))
+def test_forward_chunked_launch_order_sampled(case, subset):
+    q, k, v, _ = case.tensors()
+    o, m, l = (to_np(t) for t in run_forward(case, q, k, v))
+    o64, m64, l64 = oracle.forward_packed(q, k, v, case.cu_q, case.cu_kv, case.softmax_scale, case.causal,
+                                          heads_subset=subset)
+    for b, h in subset:
+        rows = slice(int(case.cu_q[b]), int(case.cu_q[b + 1]))
+        compare("O", o[rows, h], o64[rows, h])
+        np.testing.assert_allclose(m[rows, h], m64[rows, h], rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(l[rows, h], l64[rows, h], rtol=1e-4)
