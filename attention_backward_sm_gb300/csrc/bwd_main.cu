@@ -78,19 +78,28 @@ constexpr uint32_t COL_DV = 256;
 // mbarrier slots
 enum {
   B_KV_FULL = 0, B_KV_READY,
-  B_Q_FULL0, B_Q_FULL1, B_Q_READY0, B_Q_READY1, B_Q_EMPTY0, B_Q_EMPTY1,
-  B_DO_FULL0, B_DO_FULL1, B_DO_READY0, B_DO_READY1, B_DO_EMPTY0, B_DO_EMPTY1,
+  B_Q_FULL0, B_Q_READY0 = B_Q_FULL0 + 3, B_Q_EMPTY0 = B_Q_READY0 + 3,   // up to 3 Q stages
+  B_DO_FULL0 = B_Q_EMPTY0 + 3,
+  B_DO_FULL1, B_DO_READY0, B_DO_READY1, B_DO_EMPTY0, B_DO_EMPTY1,
   B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
   B_TEARDOWN, NUM_BARS
 };
 
-// Where the first half of a dQ partial is staged on its way to TMA: with
-// d = 128 in the block's own Q buffer (so the dS buffer is free as soon as
-// dK / dQ have run), with d = 64 in the dS buffer (measured faster there:
-// the d = 64 kernel is bound by the softmax, and releasing Q later costs
-// more than the dS hand-off).
+// Where a dQ partial lives on its way to TMA.  d = 128: tensor memory is
+// full (S, dP, dV, dK take 128 columns each), so the partial is computed
+// into the dP columns, and shared memory is full too, so it is staged half in
+// the block's own Q buffer (dead once dK has run) and half in its dO buffer
+// (dead after dV).  d = 64: the partial has 64 tensor-memory columns of its
+// own, so the next dP does not wait for it to be read out, and a 32 KB
+// staging area of its own, so no operand buffer waits for TMA to read it.
 template <int D>
-constexpr bool kStageInQ = (D == 128);
+constexpr bool kOwnDQ = (D == 64);
+// Q stages (with their row statistics).  A Q load is issued once the
+// stage's previous block has run dK and takes a few thousand cycles to land
+// behind the dQ reduce-adds on the SM's TMA engine; with d = 64 there is room
+// for a third stage, so the load has two blocks' time instead of one.
+template <int D>
+constexpr int kQStages = kOwnDQ<D> ? 3 : 2;
 
 template <int D>
 struct Layout {
@@ -98,14 +107,17 @@ struct Layout {
   static constexpr int NCH = D / 64;              // 64-column chunks per tile
   static constexpr uint32_t K = 0;
   static constexpr uint32_t V = TILE;
-  static constexpr uint32_t Q = 2 * TILE;         // 2 stages
-  static constexpr uint32_t DO = 4 * TILE;        // 2 stages
-  static constexpr uint32_t DS = 6 * TILE;        // [128 key rows, 128 query cols] bf16 = 32 KB
-  static constexpr uint32_t STATS = DS + 32768;   // per stage: lse2[128], D[128] (fp32)
-  static constexpr uint32_t BARS = STATS + 2 * 2 * 128 * 4;
+  static constexpr uint32_t Q = 2 * TILE;         // kQStages stages
+  static constexpr uint32_t DO = Q + kQStages<D> * TILE;   // 2 stages
+  static constexpr uint32_t DS = DO + 2 * TILE;   // [128 key rows, 128 query cols] bf16 = 32 KB
+  static constexpr uint32_t STG = DS + 32768;     // d = 64: dQ staging, [128 rows, 64] fp32 as 32x32 boxes
+  static constexpr uint32_t STATS = STG + (kOwnDQ<D> ? 32768 : 0);   // lse2[stage][128], then D[stage][128] (fp32)
+  static constexpr uint32_t STATS_D = STATS + kQStages<D> * 128 * 4;
+  static constexpr uint32_t BARS = STATS + kQStages<D> * 2 * 128 * 4;
   static constexpr uint32_t MISC = BARS + NUM_BARS * 8;   // abort flag, TMEM address
   static constexpr uint32_t BYTES = MISC + 16;
   static constexpr uint32_t COL_DK = COL_DV + D;
+  static constexpr uint32_t COL_DQ = kOwnDQ<D> ? COL_DV + 2 * D : COL_DP;   // dQ partial
 };
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int t) {
@@ -356,27 +368,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC + 4);
   const uint32_t bars = sbase + L::BARS;
   auto bar = [&](int i) { return bars + 8u * i; };
-  float* st_lse = reinterpret_cast<float*>(smem + L::STATS);          // [2][128]
-  float* st_D = reinterpret_cast<float*>(smem + L::STATS + 1024);     // [2][128]
+  float* st_lse = reinterpret_cast<float*>(smem + L::STATS);          // [kQStages][128]
+  float* st_D = reinterpret_cast<float*>(smem + L::STATS_D);          // [kQStages][128]
+  constexpr int NQS = kQStages<D>;
 
   if (threadIdx.x == 0) {
     *abort = 0;
     mbar_init(bar(B_KV_FULL), 1);
     mbar_init(bar(B_KV_READY), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NQS; ++s) {
       mbar_init(bar(B_Q_FULL0 + s), 1);
       mbar_init(bar(B_Q_READY0 + s), 1);
-      mbar_init(bar(B_Q_EMPTY0 + s), kStageInQ<D> ? 4 : 1);   // write-back warps, or the MMA commit
+      // released by the four write-back warps where they stage a dQ half in
+      // it (d = 128), else by the MMA commit after the block's last use
+      mbar_init(bar(B_Q_EMPTY0 + s), kOwnDQ<D> ? 1 : 4);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_DO_FULL0 + s), 1);
       mbar_init(bar(B_DO_READY0 + s), 1);
-      mbar_init(bar(B_DO_EMPTY0 + s), 4);   // one arrive per dQ write-back warp
+      mbar_init(bar(B_DO_EMPTY0 + s), kOwnDQ<D> ? 1 : 4);
     }
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_DP_FULL), 1);
     mbar_init(bar(B_P_READY), 256);
     mbar_init(bar(B_P_USED), 1);
     mbar_init(bar(B_DS_READY), 256);
-    mbar_init(bar(B_DS_FREE), kStageInQ<D> ? 1 : 4);
+    mbar_init(bar(B_DS_FREE), 1);
     mbar_init(bar(B_DQ_FULL), 1);
     mbar_init(bar(B_DQ_EMPTY), 128);
     mbar_init(bar(B_ACC_FULL), 1);
@@ -450,20 +467,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       // loads share the SM's TMA engine with the dQ reduce-adds and take
       // over a thousand cycles to land.
       for (int k = 0; ok && k < n_it; ++k) {
-        const int s = k & 1;
-        const uint32_t prev = ((k >> 1) - 1) & 1;   // parity of this stage's previous release
+        const int s = k % NQS;
+        const uint32_t use = k / NQS;               // how often stage s was filled before
+        const uint32_t prev = (use - 1) & 1;        // parity of this stage's previous release
         const int qb = qb_of(k);
         const int hq = hq_of(k);
         const int q_row0 = q_start + qb * BN;
         const int q_valid = min(BN, s1 - qb * BN);
-        if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
+        if (k >= NQS && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), L::TILE);
           for (int c = 0; c < L::NCH; ++c)
             tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, hq * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
         }
         pend_q = s;
-        par_q = (k >> 1) & 1;
+        par_q = use & 1;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           rm[j] = nm[j];
@@ -478,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           st_lse[s * 128 + lane + 32 * j] = -(rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j])));
           st_D[s * 128 + lane + 32 * j] = -rd[j];
         }
-        if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;
+        if (!mbar_wait(bar(B_Q_FULL0 + s), use & 1, abort, status)) break;
         pend_q = -1;
         if (q_valid < BN) {
           zero_rows<D>(sbase + L::Q + s * L::TILE, q_valid, lane);
@@ -532,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       constexpr uint32_t ID_KV = idesc_bf16(128, D, 0, 1);      // dV, dK: B (dO / Q) MN-major
       constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);      // dQ = dS K: both MN-major
       const uint32_t t_s = tmem + COL_S, t_dp = tmem + COL_DP;
-      const uint32_t t_dv = tmem + COL_DV, t_dk = tmem + L::COL_DK;
+      const uint32_t t_dv = tmem + COL_DV, t_dk = tmem + L::COL_DK, t_dq = tmem + L::COL_DQ;
       const uint32_t sK = sbase + L::K, sV = sbase + L::V, sDS = sbase + L::DS;
       bool ok = mbar_wait(bar(B_KV_READY), 0, abort, status) && mbar_wait(bar(B_Q_READY0), 0, abort, status);
       if (ok) {
@@ -543,46 +561,84 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         __syncwarp();
       }
+      bool dp_issued = false;   // (d = 64) dP^T of block k issued during block k-1
       for (int k = 0; ok && k < n_it; ++k) {
         const int s = k & 1;
         const uint32_t ph = k & 1;
-        const uint32_t sQ = sbase + L::Q + s * L::TILE, sDO = sbase + L::DO + s * L::TILE;
-        // dP^T into the dP columns, free once the previous dQ partial is read out.
-        if (k > 0 && !mbar_wait(bar(B_DQ_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
-        if (!mbar_wait(bar(B_DO_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
-        tc_fence_after();
-        if (elect_one()) {
-          mmas_kk<D / 16>(t_dp, sV, sDO, ID_S, 0);
-          mma_commit(bar(B_DP_FULL));
+        const int qs = k % NQS;
+        const uint32_t sQ = sbase + L::Q + qs * L::TILE, sDO = sbase + L::DO + s * L::TILE;
+        if (!dp_issued) {
+          // dP^T into the dP columns.  d = 128: they also carry the dQ
+          // partial, so they are free once the previous partial is read out.
+          // d = 64: free once the softmax has read dP of the previous block
+          // (its dS was seen ready before that block's dK / dQ were issued).
+          if (!kOwnDQ<D> && k > 0 && !mbar_wait(bar(B_DQ_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
+          if (!mbar_wait(bar(B_DO_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
+          tc_fence_after();
+          if (elect_one()) {
+            mmas_kk<D / 16>(t_dp, sV, sDO, ID_S, 0);
+            mma_commit(bar(B_DP_FULL));
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        dp_issued = false;
         // dV += P^T dO with P (bf16) read from TMEM.
         if (!mbar_wait(bar(B_P_READY), ph, abort, status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
           mmas_tm<BN / 16>(t_dv, t_s, sDO, ID_KV, k > 0);
           mma_commit(bar(B_P_USED));
+          if (kOwnDQ<D>) mma_commit(bar(B_DO_EMPTY0 + s));   // dP and dV were the dO block's uses
         }
         __syncwarp();
-        // Two independent groups follow dV_i: the next block's S^T (needs
+        // Independent groups follow dV_i: the next block's S^T (needs
         // Q_{i+1} loaded and dV_i done, since it overwrites the P columns)
         // and this block's dK / dQ (need dS_i).  Issue whichever group's
-        // inputs are ready first; dK / dQ first when both are, because the
-        // dQ partial gates the next dP through the write-back.
+        // inputs are ready first.  d = 128: dK / dQ first when both are,
+        // because the dQ partial gates the next dP through the write-back.
+        // d = 64: S^T first (the softmax needs it next), and the next
+        // block's dP^T (needs dO_{i+1} and dS_i, i.e. dP_i read) ahead of
+        // dK / dQ, which also wait for the previous dQ partial to be read
+        // out of its columns.
         {
-          bool need_s = (k + 1 < n_it), need_c2 = true;
-          const int s1n = (k + 1) & 1;
-          const uint32_t qpar = ((k + 1) >> 1) & 1;
+          bool need_s = (k + 1 < n_it), need_c2 = true, need_dp = kOwnDQ<D> && (k + 1 < n_it);
+          const int s1n = (k + 1) & 1;                    // dO stage of the next block
+          const uint32_t dpar = ((k + 1) >> 1) & 1;
+          const int q1n = (k + 1) % NQS;                  // its Q stage
+          const uint32_t qpar = ((k + 1) / NQS) & 1;
           const unsigned long long t0 = globaltimer();
           while (need_s || need_c2) {
-            bool s_ready = need_s && mbar_test(bar(B_Q_READY0 + s1n), qpar) && mbar_test(bar(B_P_USED), ph);
+            bool s_ready = need_s && mbar_test(bar(B_Q_READY0 + q1n), qpar) && mbar_test(bar(B_P_USED), ph);
             bool c_ready = need_c2 && mbar_test(bar(B_DS_READY), ph);
+            bool d_ready = false;
+            if (kOwnDQ<D>) {
+              d_ready = need_dp && c_ready && mbar_test(bar(B_DO_READY0 + s1n), dpar);
+              c_ready = c_ready && (k == 0 || mbar_test(bar(B_DQ_EMPTY), (k - 1) & 1));
+            }
             s_ready = __shfl_sync(0xffffffffu, s_ready, 0);
             c_ready = __shfl_sync(0xffffffffu, c_ready, 0);
-            if (s_ready && !c_ready) {
+            d_ready = __shfl_sync(0xffffffffu, d_ready, 0);
+            if (kOwnDQ<D> && s_ready) {
               tc_fence_after();
               if (elect_one()) {
-                mmas_kk<D / 16>(t_s, sK, sbase + L::Q + s1n * L::TILE, ID_S, 0);
+                mmas_kk<D / 16>(t_s, sK, sbase + L::Q + q1n * L::TILE, ID_S, 0);
+                mma_commit(bar(B_S_FULL));
+              }
+              __syncwarp();
+              need_s = false;
+            } else if (kOwnDQ<D> && d_ready) {
+              tc_fence_after();
+              if (elect_one()) {
+                mmas_kk<D / 16>(t_dp, sV, sbase + L::DO + s1n * L::TILE, ID_S, 0);
+                mma_commit(bar(B_DP_FULL));
+              }
+              __syncwarp();
+              need_dp = false;
+              dp_issued = true;
+            } else if (s_ready && !c_ready) {
+              tc_fence_after();
+              if (elect_one()) {
+                mmas_kk<D / 16>(t_s, sK, sbase + L::Q + q1n * L::TILE, ID_S, 0);
                 mma_commit(bar(B_S_FULL));
               }
               __syncwarp();
@@ -592,9 +648,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
               tc_fence_after();
               if (elect_one()) {
                 mmas_km<BN / 16>(t_dk, sDS, sQ, ID_KV, k > 0);
-                mmas_mm<BM / 16>(t_dp, sDS, sK, ID_DQ, 0);
+                mmas_mm<BM / 16>(t_dq, sDS, sK, ID_DQ, 0);
                 mma_commit(bar(B_DQ_FULL));
-                mma_commit(bar(kStageInQ<D> ? B_DS_FREE : B_Q_EMPTY0 + s));
+                mma_commit(bar(B_DS_FREE));
+                if (kOwnDQ<D>) mma_commit(bar(B_Q_EMPTY0 + qs));   // dK was the Q block's last use
               }
               __syncwarp();
               need_c2 = false;
@@ -633,7 +690,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int k = 0; k < n_it; ++k) {
-      const int s = k & 1;
       const uint32_t ph = k & 1;
       const int qb = qb_of(k);
       // visible query columns of key row r in this tile: [c_lo, c_lo + span)
@@ -645,13 +701,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       }
       const int span = (r < kv_valid) ? max(0, c_end - c_lo) : 0;
       const bool need_mask = __any_sync(0xffffffffu, c_lo > wg * 64 || c_lo + span < wg * 64 + 64);
-      if (!mbar_wait(bar(B_Q_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
+      const int qs = k % NQS;
+      if (!mbar_wait(bar(B_Q_READY0 + qs), (k / NQS) & 1, abort, status)) { ok = false; break; }
       // The 64 per-column statistics are read into registers before the
       // scores are waited for: shared-memory loads queue behind the MMAs'
       // operand reads, so their latency is hidden here rather than inside
       // the exp loop.
-      const float4* lse4 = reinterpret_cast<const float4*>(st_lse + s * 128 + wg * 64);
-      const float4* dvec4 = reinterpret_cast<const float4*>(st_D + s * 128 + wg * 64);
+      const float4* lse4 = reinterpret_cast<const float4*>(st_lse + qs * 128 + wg * 64);
+      const float4* dvec4 = reinterpret_cast<const float4*>(st_D + qs * 128 + wg * 64);
       float4 lsev[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) lsev[i] = lse4[i];
@@ -670,8 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 #pragma unroll
       for (int i = 0; i < 8; ++i) dv4v[i] = dvec4[i];
       if (!mbar_wait(bar(B_DP_FULL), ph, abort, status)) { ok = false; break; }
-      // The dS buffer is free once the previous block's dK / dQ MMAs ran
-      // (d = 128) or once TMA has read the dQ half staged in it (d = 64).
+      // The dS buffer is free once the previous block's dK / dQ MMAs ran.
       if (k > 0 && !mbar_wait(bar(B_DS_FREE), (k - 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t ds_row = sbase + L::DS + wg * CHUNK + (r >> 3) * 1024 + (r & 7) * 128;
@@ -717,12 +773,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     setmaxnreg_to<kRegDrain, kRegLaunch>();
     // TMEM lanes are query rows.  The partial of block k leaves as
     // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
-    // First half of the columns: staged in block k's Q buffer (d = 128; dead
-    // once dK_k has run, so the dS buffer is free for the next dS as soon as
-    // dK_k and dQ_k complete) or in the dS buffer (d = 64); second half in
-    // block k's dO buffer (dead after dV_k).  Each is released to its owner
-    // once TMA has read it.  Both halves are in flight at once; the SM's
-    // write-out bandwidth sets the pace.
+    // d = 128: first half of the columns staged in block k's Q buffer (dead
+    // once dK_k has run), second half in its dO buffer (dead after dV_k),
+    // each released to its owner once TMA has read it.  d = 64: both halves
+    // in this warp's part of the staging area.  Both halves are in flight at
+    // once; the SM's write-out bandwidth sets the pace.
     const int quarter = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     constexpr int NC = D / 32;              // 32-column chunks: 2 or 4
@@ -746,26 +801,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const int qb = qb_of(k);
       const int hq = hq_of(k);
       const int y = q_start + qb * BN + quarter * 32;
-      // The partial is staged in this block's own dO buffer and (d = 128)
-      // Q buffer or (d = 64) the dS buffer, none of which the MMAs read once
-      // dQ_i is complete; each goes back to its owner once TMA has read it.
-      const uint32_t slot_a = kStageInQ<D> ? sbase + L::Q + s * L::TILE + quarter * (L::TILE / 4)
-                                           : sbase + L::DS + quarter * 8192;
-      const uint32_t slot_b = sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
+      // d = 128: the partial is staged in this block's own Q and dO buffers,
+      // which the MMAs no longer read once dQ_i is complete; each goes back
+      // to its owner once TMA has read it.  d = 64: in this warp's 8 KB of
+      // the staging area, reused once TMA has read the previous partial.
+      const uint32_t slot_a = kOwnDQ<D> ? sbase + L::STG + quarter * 8192
+                                        : sbase + L::Q + (k % NQS) * L::TILE + quarter * (L::TILE / 4);
+      const uint32_t slot_b = kOwnDQ<D> ? slot_a + 4096 : sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
       int* ticket = det ? p.tickets + (static_cast<long long>(b * H + hq) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
       if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
       tc_fence_after();
       uint32_t va[32], vb[32], vc[32], vd[32];
-      tmem_ld32(tmem + lane_addr + COL_DP + 0, va);
-      tmem_ld32(tmem + lane_addr + COL_DP + 32, vb);
+      tmem_ld32(tmem + lane_addr + L::COL_DQ + 0, va);
+      tmem_ld32(tmem + lane_addr + L::COL_DQ + 32, vb);
       if (BPH == 2) {
-        tmem_ld32(tmem + lane_addr + COL_DP + 64, vc);
-        tmem_ld32(tmem + lane_addr + COL_DP + 96, vd);
+        tmem_ld32(tmem + lane_addr + L::COL_DQ + 64, vc);
+        tmem_ld32(tmem + lane_addr + L::COL_DQ + 96, vd);
       }
       tmem_ld_wait();
       // every TMEM column of this partial has been read
       tc_fence_before();
       mbar_arrive(bar(B_DQ_EMPTY));
+      if (kOwnDQ<D>) {
+        if (lane == 0 && issued) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+      }
       stage_box(slot_a, va);
       if (BPH == 2) stage_box(slot_a + 4096, vb);
       fence_proxy_async_smem();
@@ -805,10 +865,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 32, y);
         }
         bulk_commit();
-        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
-        mbar_arrive(bar(kStageInQ<D> ? B_Q_EMPTY0 + s : B_DS_FREE));
-        bulk_wait_read0();                                               // second half read
-        mbar_arrive(bar(B_DO_EMPTY0 + s));
+        if (!kOwnDQ<D>) {
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
+          mbar_arrive(bar(B_Q_EMPTY0 + k % NQS));
+          bulk_wait_read0();                                               // second half read
+          mbar_arrive(bar(B_DO_EMPTY0 + s));
+        }
         if (det) {
           bulk_wait_all0();                 // this block's additions are complete
           fence_proxy_async_global();
