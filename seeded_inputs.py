@@ -10,6 +10,8 @@ Recipe (all workloads are synthetic; the pages measure on no dataset):
     ``torch.Generator`` seeded with the case seed, then rounded to bf16
     (round-to-nearest-even, torch's conversion).  Each tensor uses its own
     sub-seed (seed*16 + index) so that adding a tensor never shifts another.
+    Tensors of more than 2^31 elements are drawn the same way by a seeded
+    generator on the device (bf16_normal_device).
   * Variable lengths: ``numpy.random.default_rng(seed).integers(lo, hi+1)``.
   * Packed layout ``[total, heads, head_dim]`` with cumulative int32
     offsets of B+1 entries, offsets[0] = 0 (the ``actual_q`` / ``actual_kv``
@@ -32,6 +34,19 @@ def bf16_normal(shape, seed: int, sub: int = 0) -> torch.Tensor:
     g.manual_seed(int(seed) * 16 + int(sub))
     x = torch.randn(*shape, generator=g, dtype=torch.float32)
     return x.to(torch.bfloat16)
+
+
+def bf16_normal_device(shape, seed: int, sub: int = 0, device="cuda", rows_per_draw: int = 1 << 16) -> torch.Tensor:
+    """N(0,1) float32 draws rounded to bf16, drawn on the device by its own
+    seeded generator (other values than bf16_normal for the same seed) in
+    blocks of rows, for inputs too large to draw on the host."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 16 + int(sub))
+    out = torch.empty(*shape, dtype=torch.bfloat16, device=device)
+    for r0 in range(0, shape[0], rows_per_draw):
+        r1 = min(shape[0], r0 + rows_per_draw)
+        out[r0:r1] = torch.randn(r1 - r0, *shape[1:], generator=g, device=device, dtype=torch.float32)
+    return out
 
 
 def draw_lengths(n: int, lo: int, hi: int, seed: int) -> list[int]:
