@@ -71,6 +71,7 @@ constexpr int BM = 128;   // key rows per CTA
 constexpr int BN = 128;   // query rows per block
 constexpr uint32_t CHUNK = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int kMaxRing = 64;   // key blocks per unit for the rotated deterministic order
 constexpr uint32_t COL_S = 0;
 constexpr uint32_t COL_DP = 128;
 constexpr uint32_t COL_DV = 256;
@@ -357,8 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   // starts its sweep at query block j, so a query block receives its key
   // blocks' partials one step apart (j, j-1, j-2, ... mod n), which is then
   // the fixed order of the additions; every block is added to just in time
-  // instead of all key blocks queueing on the same query block.
-  const bool rotate = p.dq_mode != 0 && !p.causal && n_qit == n_kvb;
+  // instead of all key blocks queueing on the same query block.  A block
+  // then waits on later-launched key blocks of its unit, so the unit must fit
+  // on the GPU at once: at most kMaxRing key blocks, else the ascending
+  // order (which only waits on earlier-launched blocks).  (Rotating
+  // non-square grids the same way, ties in ascending order, measured slower.)
+  const bool rotate = p.dq_mode != 0 && !p.causal && n_qit == n_kvb && n_kvb <= kMaxRing;
   const int rot = rotate ? kvb : 0;
   auto qb_of = [&](int k) { return qb0 + (k % nq_div + rot) % nq_div; };
   auto hq_of = [&](int k) { return hk * G + k / nq_div; };

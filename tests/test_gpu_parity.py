@@ -129,7 +129,7 @@ def test_single_key_degenerate(d):
 ], ids=lambda c: c.name)
 def test_deterministic_mode(case):
     """FA_DQ_DETERMINISTIC: parity with the oracle, and dQ bitwise identical
-    across runs (partials are added in ascending key-block order)."""
+    across runs (partials are added in a fixed order)."""
     import attention_backward_sm_gb300 as fab
     prep = Prepared(case)
     first = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
@@ -168,7 +168,7 @@ def test_deterministic_full_size_noncausal_bitwise():
 
 def test_deterministic_full_size_cross_bitwise():
     """Cross attention with unequal query and key block counts per sequence
-    (cfg5's lengths; rotated sweep starting at floor(j * n_q / n_k)): two
+    (cfg5's lengths; partials added in ascending key-block order): two
     deterministic runs agree bit for bit and sampled heads match the oracle."""
     import attention_backward_sm_gb300 as fab
     case = si.cfg5()
@@ -179,6 +179,33 @@ def test_deterministic_full_size_cross_bitwise():
     again = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
     for a, b in zip(first, again):
         assert torch.equal(a, b)
+
+
+def test_deterministic_unit_larger_than_the_ring_bound():
+    """160 key blocks per (sequence, head), more than the GPU holds CTAs at
+    once: the rotated order (which waits on later-launched blocks) would stall
+    here, so such units take the ascending order.  Properties that hold at any
+    size: bitwise repeats, agreement with the any-order mode up to fp32
+    summation order, and sum_j dV_j = sum_i dO_i."""
+    import attention_backward_sm_gb300 as fab
+    case = si.fixed("det_ring_d64_s20480", 1, 2, 64, 20480, 20480, False, 55)
+    q, k, v, do = (t.cuda() for t in case.tensors())
+    cu = torch.from_numpy(case.cu_q).cuda()
+    o, m, l = fab.forward_stats(q, k, v, cu, cu, case.cu_q, case.cu_kv, False, case.softmax_scale)
+    run = lambda mode: fab.backward(q, k, v, o, do, m, l, cu, cu, case.cu_q, case.cu_kv, False,
+                                    case.softmax_scale, mode)
+    first = run(fab.FA_DQ_DETERMINISTIC)
+    again = run(fab.FA_DQ_DETERMINISTIC)
+    anyorder = run(fab.FA_DQ_ATOMIC)
+    torch.cuda.synchronize()
+    fab.fa_check_device_status()
+    for a, b, c in zip(first, again, anyorder):
+        assert torch.equal(a, b)
+        a64, c64 = to_np(a), to_np(c)
+        assert np.linalg.norm(a64 - c64) <= 1e-3 * np.linalg.norm(c64)
+    dv = to_np(first[2])
+    rhs = to_np(do).sum(axis=0)
+    assert np.linalg.norm(dv.sum(axis=0) - rhs) <= 1e-2 * np.linalg.norm(rhs)
 
 
 # Causal grids whose key blocks have sweeps of very different lengths launch
