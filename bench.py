@@ -29,6 +29,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -102,7 +103,9 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # raw samples: $FA_CLOCKS_DIR if set, else the system temporary directory
+        out_dir = os.environ.get("FA_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_gpu{gpu_index}.csv")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
