@@ -7,9 +7,10 @@ memory and streams.  ``backward`` chains the three backward calls and
 allocates their outputs with torch.
 
 Tensors: q, o, do, dq are [total_q, H, d] bf16; k, v, dk, dv are
-[total_kv, H, d] bf16; m, l, D are [total_q, H] float32; cu_q / cu_kv are
-cumulative int32 offsets (B+1 entries) given both as a CUDA tensor and as a
-host sequence.
+[total_kv, Hkv, d] bf16 (Hkv divides H: grouped-query attention when it is
+smaller); m, l, D are [total_q, H] float32; d is 64, 128 or 256; cu_q /
+cu_kv are cumulative int32 offsets (B+1 entries) given both as a CUDA tensor
+and as a host sequence.
 """
 from __future__ import annotations
 
