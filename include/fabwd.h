@@ -17,7 +17,9 @@
  *
  * Conventions shared by every entry point:
  *   - Tensors are packed and contiguous.  q, o, dout, dq: [total_q, H, d];
- *     k, v, dk, dv: [total_kv, H, d]; m, l, D: [total_q, H] (float32).
+ *     k, v, dk, dv: [total_kv, H, d], or [total_kv, Hkv, d] in the entry
+ *     points that take heads_kv (grouped-query attention, Hkv divides H);
+ *     m, l, D: [total_q, H] (float32).
  *     Element type fa_bf16 is the raw 16-bit pattern of a bfloat16.
  *     The head h of row r sits at element offset (r * H + h) * d.
  *   - cu_q / cu_kv are int32 cumulative offsets with batch+1 entries,
