@@ -225,7 +225,7 @@ def fa_bwd_noalloc(q, k, v, o, do, m, l, dq, dk, dv, cu_q_dev, cu_kv_dev, cu_q_h
 
 
 def fa_selftest_wait_timeout(stream=None):
-    """Launches a block whose bounded wait runs out (about 4 s); the next
+    """Launches a block whose bounded wait runs out (after 1 s); the next
     fa_check_device_status raises FabwdError with FA_ERR_TIMEOUT."""
     _check(lib().fa_selftest_wait_timeout(_stream(stream)))
 
@@ -235,15 +235,19 @@ def fa_check_device_status(stream=None):
 
 
 def forward_stats(q, k, v, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float, stream=None,
-                  window: int = 0, bottom_right: bool = False):
+                  window: int = 0, bottom_right: bool = False, check: bool = True):
     """Allocates and returns (o, m, l) from fa_fwd_stats_ex (k, v may have
-    fewer heads than q; window > 0 is a causal sliding window)."""
+    fewer heads than q; window > 0 is a causal sliding window).  check:
+    wait for the stream and raise unless the device status word is clean
+    (a kernel whose bounded wait ran out leaves partial outputs)."""
     total_q, heads, dim = _shape(q)
     o = torch.zeros_like(q)
     m = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
     l = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
     fa_fwd_stats_ex(q, k, v, o, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask_kind(causal, bottom_right),
                     window, scale, stream)
+    if check:
+        fa_check_device_status(stream)
     return o, m, l
 
 
@@ -260,11 +264,15 @@ class Workspace:
 
 def backward(q, k, v, o, do, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
              dq_mode: int = FA_DQ_ATOMIC, out=None, work: Workspace | None = None, stream=None,
-             window: int = 0, bottom_right: bool = False):
+             window: int = 0, bottom_right: bool = False, check: bool = True):
     """preprocess -> fa_bwd_ex -> finalize on one stream; returns (dq, dk, dv).
     k and v may have fewer heads than q (grouped-query attention); the mask
     is none, causal (top-left, or bottom-right) and optionally a causal
-    sliding window of `window` keys."""
+    sliding window of `window` keys.  check (default): wait for the stream
+    and raise FabwdError unless the device status word is clean, so that
+    gradients left partial by a timed-out wait are never returned; pass
+    check=False to keep the call asynchronous and call
+    fa_check_device_status() before using the results."""
     if work is None:
         work = Workspace(q, cu_q_host, cu_kv_host, causal, dq_mode)
     if out is None:
@@ -274,24 +282,30 @@ def backward(q, k, v, o, do, m, l, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, c
     fa_bwd_ex(q, k, v, do, m, l, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host,
               mask_kind(causal, bottom_right), window, scale, dq_mode, work.ws, stream)
     fa_bwd_dq_finalize(work.dq_acc, dq, scale, stream)
+    if check:
+        fa_check_device_status(stream)
     return dq, dk, dv
 
 
 def forward_lse(q, k, v, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float, stream=None,
-                window: int = 0, bottom_right: bool = False):
-    """Allocates and returns (o, lse) from fa_fwd_lse."""
+                window: int = 0, bottom_right: bool = False, check: bool = True):
+    """Allocates and returns (o, lse) from fa_fwd_lse (check: as in
+    forward_stats)."""
     total_q, heads, dim = _shape(q)
     o = torch.zeros_like(q)
     lse = torch.zeros((total_q, heads), dtype=torch.float32, device=q.device)
     fa_fwd_lse(q, k, v, o, lse, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, mask_kind(causal, bottom_right), window,
                scale, stream)
+    if check:
+        fa_check_device_status(stream)
     return o, lse
 
 
 def backward_lse(q, k, v, o, do, lse, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, causal: bool, scale: float,
                  dq_mode: int = FA_DQ_ATOMIC, out=None, work: Workspace | None = None, stream=None,
-                 window: int = 0, bottom_right: bool = False):
-    """backward() from the single statistic lse = m + ln(l)."""
+                 window: int = 0, bottom_right: bool = False, check: bool = True):
+    """backward() from the single statistic lse = m + ln(l) (check: as in
+    backward)."""
     if work is None:
         work = Workspace(q, cu_q_host, cu_kv_host, causal, dq_mode)
     if out is None:
@@ -301,4 +315,6 @@ def backward_lse(q, k, v, o, do, lse, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host
     fa_bwd_lse(q, k, v, do, lse, work.D, work.dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host,
                mask_kind(causal, bottom_right), window, scale, dq_mode, work.ws, stream)
     fa_bwd_dq_finalize(work.dq_acc, dq, scale, stream)
+    if check:
+        fa_check_device_status(stream)
     return dq, dk, dv

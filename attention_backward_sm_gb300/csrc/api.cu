@@ -291,15 +291,18 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   return ((n * 4 + 255) / 256) * 256;
 }
 
-namespace {
+}  // extern "C"
+
+namespace fa {
 
 // Shared body of the backward entry points; stats_lse: m holds lse and l is
-// unused.
+// unused.  check_only: run every host-side check (including the device
+// check) and return before anything is launched.
 int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
              const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
              const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
              int total_kv, int heads, int heads_kv, int head_dim, int mask, int window, int stats_lse, float scale,
-             int dq_mode, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+             int dq_mode, void* workspace, size_t workspace_bytes, fa_stream_t stream, bool check_only) {
   int rc = check_shape(batch, total_q, total_kv, heads, head_dim);
   if (rc) return rc;
   if ((rc = check_groups(heads, heads_kv))) return rc;
@@ -325,6 +328,7 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
   if (need > 0 && (workspace == nullptr || workspace_bytes < need))
     return fail(FA_ERR_INVALID_ARG, "workspace of %zu bytes needed, got %zu", need, workspace_bytes);
   if ((rc = check_device())) return rc;
+  if (check_only) return ok();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (total_kv > kv_used) {
     const long long row_bytes = static_cast<long long>(heads_kv) * head_dim * 2;
@@ -382,7 +386,11 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
   return ok();
 }
 
-}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+using fa::bwd_impl;
 
 int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,
               const float* l, const float* D, float* dq_acc, fa_bf16* dk, fa_bf16* dv, const int32_t* cu_q_dev,
@@ -391,7 +399,7 @@ int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf1
               void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   return bwd_impl(q, k, v, dout, m, l, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch, total_q,
                   total_kv, heads, heads_kv, head_dim, mask, window, 0, scale, dq_mode, workspace, workspace_bytes,
-                  stream);
+                  stream, false);
 }
 
 int fa_bwd_lse(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* lse,
@@ -401,7 +409,7 @@ int fa_bwd_lse(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf
                void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   return bwd_impl(q, k, v, dout, lse, nullptr, D, dq_acc, dk, dv, cu_q_dev, cu_kv_dev, cu_q_host, cu_kv_host, batch,
                   total_q, total_kv, heads, heads_kv, head_dim, mask, window, 1, scale, dq_mode, workspace,
-                  workspace_bytes, stream);
+                  workspace_bytes, stream, false);
 }
 
 int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout, const float* m,

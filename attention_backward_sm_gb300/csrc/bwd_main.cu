@@ -960,8 +960,9 @@ cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max
 namespace {
 
 // Waits, through the kernels' own bounded mbarrier wait, on a barrier that
-// nothing arrives on: the wait gives up after its time limit and records the
-// timeout code in the status word, and the kernel returns normally.
+// nothing arrives on: the wait gives up after its time limit (1 s here,
+// shorter than the kernels' own) and records the timeout code in the
+// status word, and the kernel returns normally.
 __global__ void wait_timeout_kernel() {
   __shared__ __align__(8) uint64_t never;
   __shared__ int abort_flag;
@@ -971,7 +972,7 @@ __global__ void wait_timeout_kernel() {
     mbar_init_fence();
   }
   __syncthreads();
-  if (threadIdx.x == 0) mbar_wait(smem_u32(&never), 0, &abort_flag, &g_bwd_status);
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&never), 0, &abort_flag, &g_bwd_status, 1000000000ull);
 }
 
 }  // namespace

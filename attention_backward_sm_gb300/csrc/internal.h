@@ -99,4 +99,13 @@ inline cudaError_t set_smem_once(const void* func, int bytes, std::atomic<unsign
 // Records a message for fa_last_error() on the calling thread and returns code.
 int set_last_error(int code, const char* fmt, ...);
 
+// Shared body of fa_bwd / fa_bwd_gqa / fa_bwd_ex / fa_bwd_lse (api.cu), with
+// the arguments of fa_bwd_ex plus stats_lse (m holds lse, l unused) and
+// check_only (every host-side check, nothing launched).  Returns an fa_status.
+int bwd_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout, const float* m,
+             const float* l, const float* D, float* dq_acc, uint16_t* dk, uint16_t* dv, const int32_t* cu_q_dev,
+             const int32_t* cu_kv_dev, const int32_t* cu_q_host, const int32_t* cu_kv_host, int batch, int total_q,
+             int total_kv, int heads, int heads_kv, int head_dim, int mask, int window, int stats_lse, float scale,
+             int dq_mode, void* workspace, size_t workspace_bytes, cudaStream_t stream, bool check_only);
+
 }  // namespace fa

@@ -12,8 +12,10 @@ namespace fa {
 
 // Code a bounded wait records in the kernel's status word when it gives up.
 constexpr int kStatusTimeout = 4;
-// A bounded wait gives up after this many nanoseconds of wall time.
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+// A bounded wait gives up after this many nanoseconds of wall time: far
+// longer than any launch of these kernels runs, so that a GPU shared with
+// other work (time-sliced contexts) does not end a healthy wait.
+constexpr unsigned long long kWaitLimitNs = 20000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -79,17 +81,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up (and
-// records a timeout in *status and in *abort) after kWaitLimitNs, or as
-// soon as another thread of the CTA has set *abort.  Returns true on
-// success.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+// records a timeout in *status and in *abort) after limit_ns, or as soon
+// as another thread of the CTA has set *abort.  Returns true on success.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
 #pragma unroll 1
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       atomicCAS(status, 0, kStatusTimeout);
       *abort = 1;
       return false;

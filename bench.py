@@ -71,9 +71,14 @@ def peaks():
         return 1900.0, 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ("bwd_main.cu", "bwd_d256.cu", "sm103.cuh", "api.cu", "internal.h")
+
+
 def kernel_source_hash():
+    """Hash of every source that decides what a backward launch does (the
+    kernels, their PTX wrappers, the launch order and grid set-up)."""
     h = hashlib.sha256()
-    for f in ("bwd_main.cu", "sm103.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "attention_backward_sm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -241,6 +246,62 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def blas_threads():
+    """Threads numpy's BLAS uses in this process: threadpoolctl when it is
+    installed, else the OpenBLAS library numpy loaded, asked directly."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    import ctypes
+    paths = set()
+    try:
+        for line in open("/proc/self/maps"):
+            parts = line.split()
+            if len(parts) >= 6 and "openblas" in parts[-1].lower():
+                paths.add(parts[-1])
+    except OSError:
+        return None
+    for path in sorted(paths):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                    "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
+
+
+def single_thread_probe():
+    """Runs in a child process whose BLAS is limited to one thread: the
+    fp64 oracle backward on cfg1 (whole) and on whole units of cfg2 for up
+    to ~5 s.  Prints one JSON object."""
+    out = {"blas_threads": blas_threads()}
+    for name, budget in (("cfg1", 5.0), ("cfg2", 5.0)):
+        f, s, u = oracle_sample(make_case(name), budget)
+        out[name] = {"value": f / s / 1e12, "unit": "TFLOP/s", "units": u, "flop": f, "seconds": s}
+    print(json.dumps(out), flush=True)
+
+
+def single_thread_baseline():
+    """Oracle times at one BLAS thread on cfg1 and cfg2 (a child process, so
+    that this process keeps its full thread count)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--single-thread-probe"], env=env,
+                           capture_output=True, text=True, timeout=120)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: this is a context number
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
 def oracle_rows(case: si.Case, rows: int, b: int = 0, h: int = 0):
     """Times the fp64 oracle backward of the first `rows` query rows of one
     (sequence, head) unit against all of its keys: dQ of those rows and
@@ -294,7 +355,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {workload_desc(case)}", "sample": sample},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "blas_threads": blas_threads()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -341,16 +402,19 @@ def run_gpu(args):
     launches_per_step = 3 + (1 if args.dq_mode == 1 else 0) + (2 if case.total_kv > int(case.cu_kv[-1]) else 0)
     input_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do, o, *stats, work.dq_acc))
 
-    def step(ev=None):
-        fab.fa_bwd_preprocess(o, do, work.D, work.dq_acc)
-        if ev is not None:
-            ev[0].record(stream)
+    def bwd():
         if lse_stats:
             fab.fa_bwd_lse(q, k, v, do, stats[0], work.D, work.dq_acc, dk, dv, cu_q, cu_kv, cu_q_host, cu_kv_host,
                            mask, case.window, scale, args.dq_mode, work.ws)
         else:
             fab.fa_bwd_ex(q, k, v, do, *stats, work.D, work.dq_acc, dk, dv, cu_q, cu_kv, cu_q_host, cu_kv_host,
                           mask, case.window, scale, args.dq_mode, work.ws)
+
+    def step(ev=None):
+        fab.fa_bwd_preprocess(o, do, work.D, work.dq_acc)
+        if ev is not None:
+            ev[0].record(stream)
+        bwd()
         if ev is not None:
             ev[1].record(stream)
         fab.fa_bwd_dq_finalize(work.dq_acc, dq, scale)
@@ -361,21 +425,23 @@ def run_gpu(args):
     fab.fa_check_device_status()
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # Inputs that fit in L2 would stay cached from one step to the next: every
     # timed step is then preceded by writing a buffer four times the L2, and
     # timed by its own events.  While that write runs the host enqueues the
     # whole step, so no host-side gap falls inside the timed interval.
+    # Otherwise events at every step boundary time the steps back to back.
     small = input_bytes <= L2_BYTES
     flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=dev) if small else None
     step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps)] if small else None
+    bounds = None if small else [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     clocks = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize(dev)
-    start.record(stream)
+    if not small:
+        bounds[0].record(stream)
     for i in range(args.steps):
         if small:
             flush.zero_()
@@ -383,17 +449,47 @@ def run_gpu(args):
         step(evs[i])
         if small:
             step_evs[i][1].record(stream)
-    end.record(stream)
+        else:
+            bounds[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     if pg is not None:
         pg.barrier()
     clk = clocks.stop() if clocks else None
     fab.fa_check_device_status()
-    elapsed_ms = sum(a.elapsed_time(b) for a, b in step_evs) if small else start.elapsed_time(end)
-    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    elapsed_ms, bwd_ms = max_over_ranks([elapsed_ms, bwd_ms], pg, dev)
-    ms_per_step = elapsed_ms / args.steps
-    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    if small:
+        step_ms = [a.elapsed_time(b) for a, b in step_evs]
+    else:
+        step_ms = [bounds[i].elapsed_time(bounds[i + 1]) for i in range(args.steps)]
+    step_bwd_ms = [a.elapsed_time(b) for a, b in evs]
+    med_ms, mean_ms = statistics.median(step_ms), statistics.mean(step_ms)
+    med_ms, mean_ms = max_over_ranks([med_ms, mean_ms], pg, dev)
+    ms_per_step = med_ms
+    value = world * flops / (med_ms * 1e-3) / 1e12
+
+    # Roofline leg: fa_bwd alone.  Small inputs: the L2-flushed steps above.
+    # Otherwise a back-to-back loop of fa_bwd launches lasting at least half
+    # a second, each launch timed by its own events, with its own clock
+    # samples (a step loop of a few tens of milliseconds is too short for
+    # the nvidia-smi sampler).
+    if small:
+        bwd_times, roof_clk = step_bwd_ms, clk
+    else:
+        n_roof = max(20, int(0.5 / max(statistics.median(step_bwd_ms) * 1e-3, 1e-6)) + 1)
+        roof_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(n_roof)]
+        roof_clocks = ClockSampler(local) if rank == 0 else None
+        time.sleep(0.3 if roof_clocks else 0)
+        torch.cuda.synchronize(dev)
+        for ea, eb in roof_evs:
+            ea.record(stream)
+            bwd()
+            eb.record(stream)
+        torch.cuda.synchronize(dev)
+        roof_clk = roof_clocks.stop() if roof_clocks else None
+        fab.fa_check_device_status()
+        bwd_times = [ea.elapsed_time(eb) for ea, eb in roof_evs]
+    bwd_ms, bwd_mean_ms = statistics.median(bwd_times), statistics.mean(bwd_times)
+    bwd_ms, bwd_mean_ms = max_over_ranks([bwd_ms, bwd_mean_ms], pg, dev)
 
     # End to end through the public API from pinned host buffers.  Every step
     # copies all of its inputs host -> device, runs the backward and copies
@@ -438,7 +534,7 @@ def run_gpu(args):
                 if i >= 2:
                     s_comp.wait_event(out_done[b])             # step i-2's gradients have left dev_out[b]
                 outs = api(*dev_in[b], cu_q, cu_kv, cu_q_host, cu_kv_host, case.causal, scale, args.dq_mode,
-                           out=dev_out[b], work=work, stream=s_comp, **mask_kw(case))
+                           out=dev_out[b], work=work, stream=s_comp, check=False, **mask_kw(case))
                 comp_done[b].record(s_comp)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(comp_done[b])
@@ -455,6 +551,7 @@ def run_gpu(args):
             s_in.wait_stream(sj)
         e2.record(s_in)
         torch.cuda.synchronize(dev)
+        fab.fa_check_device_status()
         e2e_ms = s2.elapsed_time(e2) / n_e2e
         e2e_ms = max_over_ranks([e2e_ms], pg, dev)[0]
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -468,20 +565,32 @@ def run_gpu(args):
 
     peak, hbm, peak_src = peaks()
     achieved = flops / (bwd_ms * 1e-3) / 1e12
+    traffic = None if lse_stats else profiled_traffic(args.workload)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None if lse_stats else profiled_traffic(args.workload),
-                "kernel": "fa_bwd (bwd_kernel<%d>)" % case.head_dim, "fa_bwd_ms": bwd_ms,
-                "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+                "frac": achieved / peak, "traffic": traffic,
+                "hbm_gbs": None if traffic is None else traffic / (bwd_ms * 1e-3) / 1e9,
+                "hbm_frac": None if traffic is None else traffic / (bwd_ms * 1e-3) / 1e9 / hbm,
+                "kernel": "fa_bwd (bwd_kernel<%d>)" % case.head_dim if case.head_dim != 256
+                else "fa_bwd (bwd256_kernel)",
+                "fa_bwd_ms": bwd_ms, "fa_bwd_ms_mean": bwd_mean_ms, "launches_timed": len(bwd_times),
+                "timing": "median of per-launch CUDA events on the launching stream; " +
+                ("the L2-flushed steps" if small else
+                 f"{len(bwd_times)} back-to-back launches ({sum(bwd_times) / 1e3:.2f} s)"),
+                "clocks": roof_clk,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}; hbm_gbs of {peak_src}"}
 
     cpu = None
     if not args.no_cpu_baseline:
         f, s, u = oracle_sample(case, args.cpu_budget)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"fp64 backward of {u} (sequence, head) unit(s) of the workload, {f:.3e} FLOP in {s:.2f} s"}
+               "blas_threads": blas_threads(),
+               "sample": f"fp64 backward of {u} (sequence, head) unit(s) of the workload, {f:.3e} FLOP in {s:.2f} s",
+               "single_thread": single_thread_baseline()}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "ms_per_step_mean": mean_ms,
+        "value_mean": world * flops / (mean_ms * 1e-3) / 1e12, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {workload_desc(case)}", "dq_mode": args.dq_mode,
                    "statistics": "lse" if lse_stats else "m, l",
@@ -515,8 +624,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--single-thread-probe", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.single_thread_probe:
+        single_thread_probe()
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -35,9 +35,12 @@
  *     default stream) and returns FA_OK or an error code.  Arguments are
  *     checked on the host before anything is launched; on an error nothing
  *     is launched and fa_last_error() describes the problem.
- *   - Device-side waits are bounded.  A kernel whose internal wait runs out
- *     records FA_ERR_TIMEOUT in a device status word and returns early;
- *     fa_check_device_status() reads and clears it.
+ *   - Device-side waits are bounded (20 s of wall time each).  A kernel
+ *     whose internal wait runs out records FA_ERR_TIMEOUT in a device
+ *     status word and returns early, leaving its outputs incomplete;
+ *     fa_check_device_status() reads and clears the word.  A call's outputs
+ *     are valid only once a later fa_check_device_status() has returned
+ *     FA_OK (the Python binding's high-level functions do this by default).
  */
 #ifndef FABWD_H
 #define FABWD_H
@@ -85,8 +88,9 @@ enum fa_mask {
  * scaled scores and l_i = sum_j exp(scaled score - m_i) (float32) for every
  * row of every sequence.  Rows of a sequence with no keys get O = 0,
  * m = -inf, l = 0.  Padding rows are not written.  Runs on the tensor cores
- * (one CTA per 128-row query block; O accumulates in tensor memory); q, k,
- * v and o must be 16-byte aligned. */
+ * (a CTA owns one 128-row query block, or two of them at head_dim 128
+ * sharing each key/value tile; O accumulates in tensor memory); q, k, v
+ * and o must be 16-byte aligned. */
 int fa_fwd_stats(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v,
                  fa_bf16* o, float* m, float* l,
                  const int32_t* cu_q_dev, const int32_t* cu_kv_dev,
@@ -142,8 +146,13 @@ int fa_bwd_preprocess(const fa_bf16* o, const fa_bf16* dout, float* D, float* dq
                       int total_q, int heads, int head_dim, fa_stream_t stream);
 
 /* Bytes of device workspace fa_bwd needs for these shapes and dq_mode
- * (0 for FA_DQ_ATOMIC).  Returns 0 and sets fa_last_error() on bad
- * arguments, so check fa_last_error() when a mode needs workspace. */
+ * (0 for FA_DQ_ATOMIC).  The JAX cuDNN wrapper
+ * (fused_attention_stablehlo.py, _dot_product_attention_bwd_cuda_lowering)
+ * likewise returns a workspace buffer sized for the backward call, and the
+ * SK-16 article (section 6) sizes the kernel's scratch with its
+ * max_workspace_kb option; here the caller allocates it.  Returns 0 and
+ * sets fa_last_error() on bad arguments, so check fa_last_error() when a
+ * mode needs workspace. */
 size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host,
                              int batch, int heads, int head_dim, int causal, int dq_mode);
 
@@ -185,20 +194,20 @@ int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf
                int causal, float scale, int dq_mode,
                void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
-/* head_dim 256: the dK and dV accumulators of a 128-row key block would
- * fill the whole tensor memory, so two CTAs share each (sequence, key/value
- * head, key block), one per half of the head dimension; each computes the
- * full scores and dP (7/5 of the minimum matmul work) and its half of dK,
- * dV and dQ, over 64-row query blocks.  In FA_DQ_DETERMINISTIC mode the
- * workspace then holds one counter per (batch, head, 64-row query block,
- * head-dim half, 32-dim quarter); fa_bwd_workspace_size accounts for it. */
-
 /* fa_bwd_gqa with a mask and a sliding window (as in fa_fwd_stats_ex).
  * A CTA visits only the query blocks whose tiles the band of visible
  * (query, key) pairs meets; gradients of keys no query sees are exact
  * zeros.  fa_bwd and fa_bwd_gqa are this call with mask = causal and
  * window = 0.  In FA_DQ_DETERMINISTIC mode the key-block order of the dQ
- * additions is fixed for a given mask, so runs are bitwise reproducible. */
+ * additions is fixed for a given mask, so runs are bitwise reproducible.
+ *
+ * head_dim 256 (all backward entry points): the dK and dV accumulators of a
+ * 128-row key block would fill the whole tensor memory, so two CTAs share
+ * each (sequence, key/value head, key block), one per half of the head
+ * dimension; each computes the full scores and dP and its half of dK, dV
+ * and dQ, over 64-row query blocks.  In FA_DQ_DETERMINISTIC mode the
+ * workspace then holds one counter per (batch, head, 64-row query block,
+ * head-dim half, 32-dim quarter); fa_bwd_workspace_size accounts for it. */
 int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout,
               const float* m, const float* l, const float* D,
               float* dq_acc, fa_bf16* dk, fa_bf16* dv,
@@ -236,17 +245,20 @@ int fa_bwd_dq_finalize(const float* dq_acc, fa_bf16* dq, int total_q, int heads,
  * own all device memory through their own planner and give a kernel
  * library nothing but its inputs and outputs, serving loops in which an
  * allocation would stall the device, and hosts with a fixed device-memory
- * budget.  The caller passes inputs (q, k, v, o, dout, m, l,
- * offsets) and outputs (dq, dk, dv) with the layouts above.  D and the fp32
- * dQ accumulator live in one static device array of
- * FA_NOALLOC_SCRATCH_BYTES that every GPU which loads the library keeps
- * until process exit; a problem needing more (total_q * heads *
- * (head_dim + 1) * 4 bytes, rounded up) is rejected with
- * FA_ERR_INVALID_ARG before anything is launched.  The first call on a
- * device looks the array's device address up (cudaGetSymbolAddress) and
- * caches it: make that first call before any stream capture.  Every call
- * shares the array: calls whose work overlaps on the GPU race, so order
- * them on one stream.  Each call re-zeroes what must start at zero. */
+ * budget.  The caller passes inputs (q, k, v, o, dout, m, l, offsets) and
+ * outputs (dq, dk, dv) with the layouts above; head_dim 64, 128 or 256
+ * (FA_ERR_UNSUPPORTED otherwise), causal 0 or 1.  D and the fp32 dQ
+ * accumulator live in one static device array of FA_NOALLOC_SCRATCH_BYTES
+ * that every GPU which loads the library keeps until process exit; a
+ * problem needing more (total_q * heads * (head_dim + 1) * 4 bytes,
+ * rounded up) is rejected with FA_ERR_INVALID_ARG.  Every argument is
+ * checked before anything is launched.  Each call looks up the array's
+ * device address in the current context (cudaGetSymbolAddress), so it
+ * stays valid across context switches and device resets; the first call in
+ * a context loads the library's device code, so make it before any stream
+ * capture.  Every call shares the array: calls whose work overlaps on the
+ * GPU race, so order them on one stream.  Each call re-zeroes what must
+ * start at zero. */
 int fa_bwd_noalloc(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* o,
                    const fa_bf16* dout, const float* m, const float* l,
                    fa_bf16* dq, fa_bf16* dk, fa_bf16* dv,
@@ -257,7 +269,8 @@ int fa_bwd_noalloc(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const f
 
 /* Diagnostic (the pages have no counterpart): launches one block that
  * waits, through the same bounded mbarrier wait the kernels use, on a
- * barrier nothing arrives on.  After the wait's time limit (4 s) it records
+ * barrier nothing arrives on.  After its own short limit (1 s; the
+ * kernels' waits give up after 20 s) it records
  * FA_ERR_TIMEOUT in the device status word and returns; nothing faults and
  * the context stays usable.  The next fa_check_device_status on `stream`
  * then returns FA_ERR_TIMEOUT.  Lets a caller test its handling of a timed
@@ -265,12 +278,18 @@ int fa_bwd_noalloc(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const f
 int fa_selftest_wait_timeout(fa_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device status word
- * that bounded waits set.  Returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_CUDA. */
+ * that bounded waits set.  Returns FA_OK, FA_ERR_TIMEOUT or FA_ERR_CUDA.
+ * The outputs of the kernels launched before it are complete and valid
+ * only when it returns FA_OK: after FA_ERR_TIMEOUT some CTAs stopped early
+ * and dq_acc, dk, dv (or o, m, l) may be partial. */
 int fa_check_device_status(fa_stream_t stream);
 
 /* Message describing the last error returned on the calling thread
- * (empty string after success).  The pointer stays valid until the next
- * call on the same thread. */
+ * (empty string after success), in the manner of the argument validators
+ * of the PyPTO block_attn_res_impl.py page (_validate_forward_inputs:
+ * which argument, what was expected, what was given) and of the JAX
+ * wrapper's check_layout.  The pointer stays valid until the next call on
+ * the same thread. */
 const char* fa_last_error(void);
 
 #ifdef __cplusplus

@@ -160,3 +160,39 @@ def test_lse_entry_points_need_no_l(lib):
     hp = z.ctypes.data_as(ctypes.c_void_p)
     assert lib.fa_bwd_lse(None, None, None, None, None, None, None, None, None, None, None, hp, hp, 0, 0, 0,
                           2, 2, 128, 1, 0, 0.1, 0, None, 0, None) == 0
+
+
+def _call_noalloc(lib, cu_q, cu_kv, heads=2, head_dim=128, causal=0, total_q=None, total_kv=None, scale=0.1,
+                  ptr=16):
+    p = ctypes.c_void_p(ptr)   # never dereferenced: the checks fail first
+    total_q = int(cu_q[-1]) if total_q is None else total_q
+    total_kv = int(cu_kv[-1]) if total_kv is None else total_kv
+    return lib.fa_bwd_noalloc(p, p, p, p, p, p, p, p, p, p, p, p, cu_q.ctypes.data_as(ctypes.c_void_p),
+                              cu_kv.ctypes.data_as(ctypes.c_void_p), len(cu_q) - 1, total_q, total_kv, heads,
+                              head_dim, causal, scale, None)
+
+
+def test_noalloc_checks_every_argument_before_any_cuda_call(lib):
+    """fa_bwd_noalloc rejects bad arguments with the same codes as fa_bwd
+    before it touches CUDA at all (here there is no GPU, so any CUDA call
+    would turn into FA_ERR_CUDA instead)."""
+    good = _offsets(0, 10, 30)
+    assert _call_noalloc(lib, _offsets(0, 40, 30), good, total_q=40) == 1    # decreasing offsets
+    assert b"non-decreasing" in lib.fa_last_error()
+    assert _call_noalloc(lib, _offsets(1, 10, 30), good) == 1                # cu[0] != 0
+    assert _call_noalloc(lib, good, _offsets(0, 10, 50), total_kv=30) == 1   # offsets past the tensor
+    assert _call_noalloc(lib, good, good, head_dim=96) == 2                  # FA_ERR_UNSUPPORTED
+    assert _call_noalloc(lib, good, good, causal=2) == 1
+    assert _call_noalloc(lib, good, good, scale=float("nan")) == 1
+    assert _call_noalloc(lib, good, good, ptr=8) == 1                        # misaligned pointers
+    assert b"aligned" in lib.fa_last_error()
+    # too large for the fixed array: total_q * heads * (head_dim + 1) * 4 > 16 MiB
+    big = _offsets(0, 40000)
+    assert _call_noalloc(lib, big, _offsets(0, 8), heads=8, head_dim=256) == 1
+    assert b"scratch" in lib.fa_last_error()
+    # head_dim 256 passes the shape checks: it then stops at a NULL device
+    # pointer (INVALID_ARG), not at the head dimension (UNSUPPORTED)
+    p = ctypes.c_void_p(16)
+    hp = good.ctypes.data_as(ctypes.c_void_p)
+    rc = lib.fa_bwd_noalloc(None, p, p, p, p, p, p, p, p, p, p, p, hp, hp, 2, 30, 30, 2, 256, 0, 0.1, None)
+    assert rc == 1 and b"NULL" in lib.fa_last_error()
