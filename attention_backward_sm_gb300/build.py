@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libfabwd.so")
-SOURCES = ["api.cu", "small_kernels.cu", "fwd_main.cu", "bwd_main.cu", "bwd_d256.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "small_kernels.cu", "fwd_main.cu", "bwd_main.cu", "bwd_d256.cu", "dq_main.cu", "noalloc.cu"]
 HEADERS = ["internal.h", "sm103.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -268,7 +268,9 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   (void)cu_kv_host;
   (void)causal;
   if (check_shape(batch, 0, 0, heads, head_dim)) return 0;
-  if (dq_mode == FA_DQ_ATOMIC) {
+  // Atomic mode, and the deterministic mode at head_dim 64 and 128 (whose
+  // dQ comes from a kernel that sums every row in one CTA), need none.
+  if (dq_mode == FA_DQ_ATOMIC || (dq_mode == FA_DQ_DETERMINISTIC && head_dim != 256)) {
     ok();
     return 0;
   }
@@ -283,11 +285,9 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   int max_q = 0;
   for (int b = 0; b < batch; ++b) max_q = cu_q_host[b + 1] - cu_q_host[b] > max_q ? cu_q_host[b + 1] - cu_q_host[b] : max_q;
   ok();
-  // one int32 counter per (batch, head, 128-row query block, 32-row quarter); with
-  // head_dim 256 per (batch, head, 64-row query block, head-dim half, 32-dim quarter);
-  // rounded to 256 B
-  const size_t n = head_dim == 256 ? static_cast<size_t>(batch) * heads * ((max_q + 63) / 64) * 8
-                                   : static_cast<size_t>(batch) * heads * ((max_q + 127) / 128) * 4;
+  // head_dim 256: one int32 counter per (batch, head, 64-row query block,
+  // head-dim half, 32-dim quarter), rounded to 256 B
+  const size_t n = static_cast<size_t>(batch) * heads * ((max_q + 63) / 64) * 8;
   return ((n * 4 + 255) / 256) * 256;
 }
 
@@ -372,16 +372,25 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
   p.stats_lse = stats_lse;
   p.dq_mode = dq_mode;
   p.max_q_blocks = (max_q + q_box - 1) / q_box;
-  p.kv_reverse = (dq_mode == FA_DQ_DETERMINISTIC && causal) ? 1 : 0;
+  p.kv_reverse = (head_dim == 256 && dq_mode == FA_DQ_DETERMINISTIC && causal) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tickets = static_cast<int*>(workspace);
-  if (dq_mode == FA_DQ_DETERMINISTIC) {
+  if (need > 0) {
     cudaError_t e = fa::launch_zero_fill(workspace, static_cast<long long>(need), s);
     if (e != cudaSuccess) return cuda_fail(e, "ticket reset");
   }
-  cudaError_t e = head_dim == 256 ? fa::launch_bwd256(p, batch, (max_kv + 127) / 128, s)
-                                   : fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, s);
+  cudaError_t e;
+  if (head_dim == 256) {
+    e = fa::launch_bwd256(p, batch, (max_kv + 127) / 128, s);
+  } else if (dq_mode == FA_DQ_ATOMIC) {
+    e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, true, s);
+  } else {
+    // deterministic: dK and dV from the key-block-outer kernel, dQ from the
+    // query-block-outer one (each row summed by one CTA in a fixed order)
+    e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, false, s);
+    if (e == cudaSuccess && max_q > 0) e = fa::launch_dq(p, head_dim, batch, max_kv, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
   return ok();
 }
@@ -458,11 +467,13 @@ int fa_selftest_wait_timeout(fa_stream_t stream) {
 }
 
 int fa_check_device_status(fa_stream_t stream) {
-  int st = 0, st256 = 0, st_fwd = 0;
+  int st = 0, st256 = 0, st_dq = 0, st_fwd = 0;
   int e = fa::bwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st);
   if (e == 0) e = fa::bwd256_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st256);
+  if (e == 0) e = fa::dq_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st_dq);
   if (e == 0) e = fa::fwd_read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &st_fwd);
   if (st == 0) st = st256;
+  if (st == 0) st = st_dq;
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "fa_check_device_status");
   if (st == 4) return fail(FA_ERR_TIMEOUT, "a device-side wait in fa_bwd ran out of time (status %d)", st);
   if (st != 0) return fail(FA_ERR_CUDA, "fa_bwd recorded device status %d", st);

@@ -71,7 +71,6 @@ constexpr int BM = 128;   // key rows per CTA
 constexpr int BN = 128;   // query rows per block
 constexpr uint32_t CHUNK = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int kMaxRing = 64;   // key blocks per unit for the rotated deterministic order
 constexpr uint32_t COL_S = 0;
 constexpr uint32_t COL_DP = 128;
 constexpr uint32_t COL_DV = 256;
@@ -291,9 +290,16 @@ __device__ __forceinline__ int floordiv(long long a, int b) {
   return static_cast<int>(q);
 }
 
-template <int D, bool kChunked>
+// kDQ: also compute the dQ partials and add them into dq_acc (any order);
+// without it the kernel computes dK and dV only (the deterministic mode,
+// whose dQ comes from dq_kernel), and the dP columns, the Q buffers and
+// the dO buffers are released as soon as the MMAs are done with them.
+template <int D, bool kChunked, bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
+  // dP columns, Q and dO buffers free of dQ partials (d = 64 keeps its
+  // partial in columns and a staging area of its own)
+  constexpr bool kSep = kOwnDQ<D> || !kDQ;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
 
@@ -305,13 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   // with the key block as the slow index within a chunk, so under a causal
   // mask the long sweeps of the low key blocks start first and the short ones
   // fill the tail, while the chunk's query-side data stays in L2.
-  // Deterministic causal runs add dQ partials in descending key-block order
-  // and launch key blocks high to low (head_chunk = 1), so that every CTA a
-  // CTA waits for was launched before it (see the dQ write-back).
   int kvb, hk, b;
   if constexpr (!kChunked) {
-    kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                       : static_cast<int>(blockIdx.x);
+    kvb = static_cast<int>(blockIdx.x);
     hk = blockIdx.y;
     b = blockIdx.z;
   } else {
@@ -352,20 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                                         : n_qb - 1;
   const int n_qit = max(0, qb_hi - qb0 + 1);        // query blocks per query head
   const int n_it = G * n_qit;                       // iterations of the sweep
-  const int n_kvb = (s2 + BM - 1) / BM;
   const int nq_div = max(1, n_qit);                 // divisor that stays valid when there is no work
-  // Deterministic dQ without a mask on a square block grid: key block j
-  // starts its sweep at query block j, so a query block receives its key
-  // blocks' partials one step apart (j, j-1, j-2, ... mod n), which is then
-  // the fixed order of the additions; every block is added to just in time
-  // instead of all key blocks queueing on the same query block.  A block
-  // then waits on later-launched key blocks of its unit, so the unit must fit
-  // on the GPU at once: at most kMaxRing key blocks, else the ascending
-  // order (which only waits on earlier-launched blocks).  (Rotating
-  // non-square grids the same way, ties in ascending order, measured slower.)
-  const bool rotate = p.dq_mode != 0 && !p.causal && n_qit == n_kvb && n_kvb <= kMaxRing;
-  const int rot = rotate ? kvb : 0;
-  auto qb_of = [&](int k) { return qb0 + (k % nq_div + rot) % nq_div; };
+  auto qb_of = [&](int k) { return qb0 + k % nq_div; };
   auto hq_of = [&](int k) { return hk * G + k / nq_div; };
   const long long rs_kv = static_cast<long long>(p.heads_kv) * D;   // key-side row stride (elements)
 
@@ -386,12 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       mbar_init(bar(B_Q_READY0 + s), 1);
       // released by the four write-back warps where they stage a dQ half in
       // it (d = 128), else by the MMA commit after the block's last use
-      mbar_init(bar(B_Q_EMPTY0 + s), kOwnDQ<D> ? 1 : 4);
+      mbar_init(bar(B_Q_EMPTY0 + s), kSep ? 1 : 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_DO_FULL0 + s), 1);
       mbar_init(bar(B_DO_READY0 + s), 1);
-      mbar_init(bar(B_DO_EMPTY0 + s), kOwnDQ<D> ? 1 : 4);
+      mbar_init(bar(B_DO_EMPTY0 + s), kSep ? 1 : 4);
     }
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_DP_FULL), 1);
@@ -577,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           // partial, so they are free once the previous partial is read out.
           // d = 64: free once the softmax has read dP of the previous block
           // (its dS was seen ready before that block's dK / dQ were issued).
-          if (!kOwnDQ<D> && k > 0 && !mbar_wait(bar(B_DQ_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
+          if (!kSep && k > 0 && !mbar_wait(bar(B_DQ_EMPTY), (k - 1) & 1, abort, status)) { ok = false; break; }
           if (!mbar_wait(bar(B_DO_READY0 + s), (k >> 1) & 1, abort, status)) { ok = false; break; }
           tc_fence_after();
           if (elect_one()) {
@@ -593,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         if (elect_one()) {
           mmas_tm<BN / 16>(t_dv, t_s, sDO, ID_KV, k > 0);
           mma_commit(bar(B_P_USED));
-          if (kOwnDQ<D>) mma_commit(bar(B_DO_EMPTY0 + s));   // dP and dV were the dO block's uses
+          if (kSep) mma_commit(bar(B_DO_EMPTY0 + s));   // dP and dV were the dO block's uses
         }
         __syncwarp();
         // Independent groups follow dV_i: the next block's S^T (needs
@@ -606,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         // dK / dQ, which also wait for the previous dQ partial to be read
         // out of its columns.
         {
-          bool need_s = (k + 1 < n_it), need_c2 = true, need_dp = kOwnDQ<D> && (k + 1 < n_it);
+          bool need_s = (k + 1 < n_it), need_c2 = true, need_dp = kSep && (k + 1 < n_it);
           const int s1n = (k + 1) & 1;                    // dO stage of the next block
           const uint32_t dpar = ((k + 1) >> 1) & 1;
           const int q1n = (k + 1) % NQS;                  // its Q stage
@@ -616,14 +606,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             bool s_ready = need_s && mbar_test(bar(B_Q_READY0 + q1n), qpar) && mbar_test(bar(B_P_USED), ph);
             bool c_ready = need_c2 && mbar_test(bar(B_DS_READY), ph);
             bool d_ready = false;
-            if (kOwnDQ<D>) {
+            if (kSep) {
               d_ready = need_dp && c_ready && mbar_test(bar(B_DO_READY0 + s1n), dpar);
-              c_ready = c_ready && (k == 0 || mbar_test(bar(B_DQ_EMPTY), (k - 1) & 1));
+              if (kDQ) c_ready = c_ready && (k == 0 || mbar_test(bar(B_DQ_EMPTY), (k - 1) & 1));
             }
             s_ready = __shfl_sync(0xffffffffu, s_ready, 0);
             c_ready = __shfl_sync(0xffffffffu, c_ready, 0);
             d_ready = __shfl_sync(0xffffffffu, d_ready, 0);
-            if (kOwnDQ<D> && s_ready) {
+            if (kSep && s_ready) {
               tc_fence_after();
               if (elect_one()) {
                 mmas_kk<D / 16>(t_s, sK, sbase + L::Q + q1n * L::TILE, ID_S, 0);
@@ -631,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
               }
               __syncwarp();
               need_s = false;
-            } else if (kOwnDQ<D> && d_ready) {
+            } else if (kSep && d_ready) {
               tc_fence_after();
               if (elect_one()) {
                 mmas_kk<D / 16>(t_dp, sV, sbase + L::DO + s1n * L::TILE, ID_S, 0);
@@ -653,10 +643,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
               tc_fence_after();
               if (elect_one()) {
                 mmas_km<BN / 16>(t_dk, sDS, sQ, ID_KV, k > 0);
-                mmas_mm<BM / 16>(t_dq, sDS, sK, ID_DQ, 0);
-                mma_commit(bar(B_DQ_FULL));
+                if (kDQ) {
+                  mmas_mm<BM / 16>(t_dq, sDS, sK, ID_DQ, 0);
+                  mma_commit(bar(B_DQ_FULL));
+                }
                 mma_commit(bar(B_DS_FREE));
-                if (kOwnDQ<D>) mma_commit(bar(B_Q_EMPTY0 + qs));   // dK was the Q block's last use
+                if (kSep) mma_commit(bar(B_Q_EMPTY0 + qs));   // dK was the Q block's last use
               }
               __syncwarp();
               need_c2 = false;
@@ -776,117 +768,92 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ write-back
     setmaxnreg_to<kRegDrain, kRegLaunch>();
-    // TMEM lanes are query rows.  The partial of block k leaves as
-    // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
-    // d = 128: first half of the columns staged in block k's Q buffer (dead
-    // once dK_k has run), second half in its dO buffer (dead after dV_k),
-    // each released to its owner once TMA has read it.  d = 64: both halves
-    // in this warp's part of the staging area.  Both halves are in flight at
-    // once; the SM's write-out bandwidth sets the pace.
-    const int quarter = warp & 3;
-    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    constexpr int NC = D / 32;              // 32-column chunks: 2 or 4
-    constexpr int BPH = NC / 2;             // boxes per warp per half: 1 or 2
-    auto stage_box = [&](uint32_t box, const uint32_t (&v)[32]) {
-      const uint32_t row = box + lane * 128;
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-    };
-    // Deterministic mode: the (query block, quarter) partials of a head are
-    // added in ascending key-block order.  Key block j waits until the
-    // counter of its rows reads j, sends both halves, waits for them to
-    // complete and then advances the counter.  Every earlier key block of
-    // the head was launched before this one and never waits on a later one.
-    const bool det = p.dq_mode != 0;
-    bool issued = false;
+    if constexpr (kDQ) {
+      // TMEM lanes are query rows.  The partial of block k leaves as
+      // 128B-swizzled [32 x 32] fp32 boxes reduce-added into dq_acc by TMA.
+      // d = 128: first half of the columns staged in block k's Q buffer (dead
+      // once dK_k has run), second half in its dO buffer (dead after dV_k),
+      // each released to its owner once TMA has read it.  d = 64: both halves
+      // in this warp's part of the staging area.  Both halves are in flight at
+      // once; the SM's write-out bandwidth sets the pace.
+      const int quarter = warp & 3;
+      const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+      constexpr int NC = D / 32;              // 32-column chunks: 2 or 4
+      constexpr int BPH = NC / 2;             // boxes per warp per half: 1 or 2
+      auto stage_box = [&](uint32_t box, const uint32_t (&v)[32]) {
+        const uint32_t row = box + lane * 128;
+  #pragma unroll
+        for (int g = 0; g < 8; ++g)
+          st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+      };
+      bool issued = false;
 
-    for (int k = 0; k < n_it; ++k) {
-      const int s = k & 1;
-      const int qb = qb_of(k);
-      const int hq = hq_of(k);
-      const int y = q_start + qb * BN + quarter * 32;
-      // d = 128: the partial is staged in this block's own Q and dO buffers,
-      // which the MMAs no longer read once dQ_i is complete; each goes back
-      // to its owner once TMA has read it.  d = 64: in this warp's 8 KB of
-      // the staging area, reused once TMA has read the previous partial.
-      const uint32_t slot_a = kOwnDQ<D> ? sbase + L::STG + quarter * 8192
-                                        : sbase + L::Q + (k % NQS) * L::TILE + quarter * (L::TILE / 4);
-      const uint32_t slot_b = kOwnDQ<D> ? slot_a + 4096 : sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
-      int* ticket = det ? p.tickets + (static_cast<long long>(b * H + hq) * p.max_q_blocks + qb) * 4 + quarter : nullptr;
-      if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
-      tc_fence_after();
-      uint32_t va[32], vb[32], vc[32], vd[32];
-      tmem_ld32(tmem + lane_addr + L::COL_DQ + 0, va);
-      tmem_ld32(tmem + lane_addr + L::COL_DQ + 32, vb);
-      if (BPH == 2) {
-        tmem_ld32(tmem + lane_addr + L::COL_DQ + 64, vc);
-        tmem_ld32(tmem + lane_addr + L::COL_DQ + 96, vd);
-      }
-      tmem_ld_wait();
-      // every TMEM column of this partial has been read
-      tc_fence_before();
-      mbar_arrive(bar(B_DQ_EMPTY));
-      if (kOwnDQ<D>) {
-        if (lane == 0 && issued) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      for (int k = 0; k < n_it; ++k) {
+        const int s = k & 1;
+        const int qb = qb_of(k);
+        const int hq = hq_of(k);
+        const int y = q_start + qb * BN + quarter * 32;
+        // d = 128: the partial is staged in this block's own Q and dO buffers,
+        // which the MMAs no longer read once dQ_i is complete; each goes back
+        // to its owner once TMA has read it.  d = 64: in this warp's 8 KB of
+        // the staging area, reused once TMA has read the previous partial.
+        const uint32_t slot_a = kOwnDQ<D> ? sbase + L::STG + quarter * 8192
+                                          : sbase + L::Q + (k % NQS) * L::TILE + quarter * (L::TILE / 4);
+        const uint32_t slot_b = kOwnDQ<D> ? slot_a + 4096 : sbase + L::DO + s * L::TILE + quarter * (L::TILE / 4);
+        if (!mbar_wait(bar(B_DQ_FULL), k & 1, abort, status)) break;
+        tc_fence_after();
+        uint32_t va[32], vb[32], vc[32], vd[32];
+        tmem_ld32(tmem + lane_addr + L::COL_DQ + 0, va);
+        tmem_ld32(tmem + lane_addr + L::COL_DQ + 32, vb);
+        if (BPH == 2) {
+          tmem_ld32(tmem + lane_addr + L::COL_DQ + 64, vc);
+          tmem_ld32(tmem + lane_addr + L::COL_DQ + 96, vd);
+        }
+        tmem_ld_wait();
+        // every TMEM column of this partial has been read
+        tc_fence_before();
+        mbar_arrive(bar(B_DQ_EMPTY));
+        if (kOwnDQ<D>) {
+          if (lane == 0 && issued) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+        }
+        stage_box(slot_a, va);
+        if (BPH == 2) stage_box(slot_a + 4096, vb);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&p.tm_dq, slot_a, hq * D + 0, y);
+          if (BPH == 2) tma_reduce_add_2d(&p.tm_dq, slot_a + 4096, hq * D + 32, y);
+          bulk_commit();
+          issued = true;
+        }
+        if (BPH == 2) {
+          stage_box(slot_b, vc);
+          stage_box(slot_b + 4096, vd);
+        } else {
+          stage_box(slot_b, vb);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (BPH == 2) {
+            tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 64, y);
+            tma_reduce_add_2d(&p.tm_dq, slot_b + 4096, hq * D + 96, y);
+          } else {
+            tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 32, y);
+          }
+          bulk_commit();
+          if (!kOwnDQ<D>) {
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
+            mbar_arrive(bar(B_Q_EMPTY0 + k % NQS));
+            bulk_wait_read0();                                               // second half read
+            mbar_arrive(bar(B_DO_EMPTY0 + s));
+          }
+        }
         __syncwarp();
       }
-      stage_box(slot_a, va);
-      if (BPH == 2) stage_box(slot_a + 4096, vb);
-      fence_proxy_async_smem();
-      __syncwarp();
-      bool turn = true;
-      if (lane == 0 && det) {
-        // partials that come before this one: those of the key blocks
-        // kb_lo..kvb-1 (ascending order) or kvb+1..kb_hi (descending order),
-        // [kb_lo, kb_hi] being the key blocks whose tiles with query block qb
-        // the mask band meets
-        const long long q0 = static_cast<long long>(qb) * BN;
-        const int kb_hi = p.causal ? min(n_kvb - 1, floordiv(q0 + BN - 1 + off, BM)) : n_kvb - 1;
-        const int kb_lo = (p.causal && W > 0) ? max(0, floordiv(q0 + off - W + 1, BM)) : 0;
-        const int before = rotate ? (qb - kvb + n_kvb) % n_kvb : p.kv_reverse ? kb_hi - kvb : kvb - kb_lo;
-        turn = wait_counter(ticket, before, abort, status);
-        fence_proxy_async_global();
-      }
-      if (lane == 0 && turn) {
-        tma_reduce_add_2d(&p.tm_dq, slot_a, hq * D + 0, y);
-        if (BPH == 2) tma_reduce_add_2d(&p.tm_dq, slot_a + 4096, hq * D + 32, y);
-        bulk_commit();
-        issued = true;
-      }
-      if (BPH == 2) {
-        stage_box(slot_b, vc);
-        stage_box(slot_b + 4096, vd);
-      } else {
-        stage_box(slot_b, vb);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && turn) {
-        if (BPH == 2) {
-          tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 64, y);
-          tma_reduce_add_2d(&p.tm_dq, slot_b + 4096, hq * D + 96, y);
-        } else {
-          tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 32, y);
-        }
-        bulk_commit();
-        if (!kOwnDQ<D>) {
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
-          mbar_arrive(bar(B_Q_EMPTY0 + k % NQS));
-          bulk_wait_read0();                                               // second half read
-          mbar_arrive(bar(B_DO_EMPTY0 + s));
-        }
-        if (det) {
-          bulk_wait_all0();                 // this block's additions are complete
-          fence_proxy_async_global();
-          __threadfence();
-          atomicAdd(ticket, 1);
-        }
-      }
-      if (__any_sync(0xffffffffu, lane == 0 && !turn)) break;
-      __syncwarp();
+      if (lane == 0 && issued) bulk_wait_all0();
     }
-    if (lane == 0 && issued) bulk_wait_all0();
   } else {
     setmaxnreg_to<kRegOther, kRegLaunch>();   // warp 3 only waits at the final barrier
   }
@@ -899,24 +866,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   }
 }
 
-template <int D>
+template <int D, bool kDQ>
 cudaError_t launch_d(const BwdParams& p, int batch, int max_kv_blocks, cudaStream_t s) {
   constexpr uint32_t bytes = Layout<D>::BYTES;
   static_assert(bytes <= 232448, "shared memory budget");
   static std::atomic<unsigned long long> smem_set{0}, smem_set_chunked{0};
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D, false>), (int)bytes, smem_set);
-  if (e == cudaSuccess) e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D, true>), (int)bytes, smem_set_chunked);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D, false, kDQ>), (int)bytes, smem_set);
+  if (e == cudaSuccess)
+    e = set_smem_once(reinterpret_cast<const void*>(bwd_kernel<D, true, kDQ>), (int)bytes, smem_set_chunked);
   if (e != cudaSuccess) return e;
   if (static_cast<long long>(max_kv_blocks) * p.heads_kv * batch > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   BwdParams q = p;
   q.batch = batch;
   q.grid_kv = max_kv_blocks;
-  q.head_chunk = launch_head_chunk(p, batch, max_kv_blocks, BM, BN, D);
+  // neither variant orders its CTAs' work: the launch order is free
+  BwdParams any_order = p;
+  any_order.dq_mode = 0;
+  q.head_chunk = launch_head_chunk(any_order, batch, max_kv_blocks, BM, BN, D);
   dim3 grid(max_kv_blocks, p.heads_kv, batch);
   if (q.head_chunk > 1)
-    bwd_kernel<D, true><<<grid, kThreads, bytes, s>>>(q);
+    bwd_kernel<D, true, kDQ><<<grid, kThreads, bytes, s>>>(q);
   else
-    bwd_kernel<D, false><<<grid, kThreads, bytes, s>>>(q);
+    bwd_kernel<D, false, kDQ><<<grid, kThreads, bytes, s>>>(q);
   return cudaGetLastError();
 }
 
@@ -952,9 +923,12 @@ int launch_head_chunk(const BwdParams& p, int batch, int n_kvb, int bm, int bn, 
   return static_cast<int>(std::max(1LL, std::min<long long>(static_cast<long long>(p.heads_kv) * batch, kChunkBytes / unit_bytes)));
 }
 
-cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, cudaStream_t s) {
+cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, bool with_dq,
+                            cudaStream_t s) {
   if (batch <= 0 || max_kv_blocks <= 0) return cudaSuccess;
-  return head_dim == 64 ? launch_d<64>(p, batch, max_kv_blocks, s) : launch_d<128>(p, batch, max_kv_blocks, s);
+  if (with_dq)
+    return head_dim == 64 ? launch_d<64, true>(p, batch, max_kv_blocks, s) : launch_d<128, true>(p, batch, max_kv_blocks, s);
+  return head_dim == 64 ? launch_d<64, false>(p, batch, max_kv_blocks, s) : launch_d<128, false>(p, batch, max_kv_blocks, s);
 }
 
 namespace {

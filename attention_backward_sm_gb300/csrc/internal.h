@@ -27,7 +27,8 @@ struct BwdParams {
   uint16_t* dv;
   const int32_t* cu_q;
   const int32_t* cu_kv;
-  int* tickets;        // deterministic mode: one counter per (batch, head, query block, 32-row quarter)
+  int* tickets;        // deterministic mode at head_dim 256: one counter per (batch, head, 64-row query
+                       // block, head-dim half, 32-dim quarter)
   int heads;           // query heads
   int heads_kv;        // key/value heads (heads is a multiple of it)
   int causal;          // 1: causal mask (top-left unless bottom_right)
@@ -36,7 +37,7 @@ struct BwdParams {
   int stats_lse;       // 1: m holds lse = m + ln(l) per row and l is unused
   int dq_mode;
   int max_q_blocks;    // query blocks of the longest query sequence
-  int kv_reverse;      // 1: key blocks are launched from the last one down
+  int kv_reverse;      // 1: key blocks are launched from the last one down (head_dim 256, deterministic)
   int batch;           // sequences
   int grid_kv;         // key blocks of the longest key sequence (launched per head)
   int head_chunk;      // (sequence, key/value head) units per launch-order chunk
@@ -44,7 +45,14 @@ struct BwdParams {
   float scale_log2;    // scale * log2(e)
 };
 
-cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, cudaStream_t s);
+// head_dim 64 / 128 key-block-outer kernel; with_dq: also add the dQ
+// partials into dq_acc (atomic mode), else dK and dV only.
+cudaError_t launch_bwd_main(const BwdParams& p, int head_dim, int batch, int max_kv_blocks, bool with_dq,
+                            cudaStream_t s);
+// head_dim 64 / 128 deterministic dQ (dq_main.cu): stores the unscaled
+// dS K sums of every query row into dq_acc, one CTA per query block.
+cudaError_t launch_dq(const BwdParams& p, int head_dim, int batch, int max_kv, cudaStream_t s);
+int dq_read_and_clear_status(cudaStream_t s, int* status);
 // (sequence, key/value head) units per launch-order chunk of a backward grid
 // with n_kvb key blocks of bm rows and query blocks of bn rows.
 int launch_head_chunk(const BwdParams& p, int batch, int n_kvb, int bm, int bn, int head_dim);

@@ -123,13 +123,14 @@ def test_single_key_degenerate(d):
 @pytest.mark.parametrize("case", [
     si.fixed("det_d128_causal_tail", 2, 3, 128, 700, 700, True, 51),
     si.Case("det_d64_varlen_cross", 3, 64, [300, 1, 513], [257, 700, 129], False, 52, pad_q=5, pad_kv=3),
-    # square without a mask: key blocks sweep the query blocks in rotated order
     si.fixed("det_d128_noncausal_square_tail", 2, 3, 128, 700, 700, False, 53),
     si.fixed("det_d64_noncausal_square", 1, 2, 64, 1024, 1024, False, 54, heads_kv=1),
 ], ids=lambda c: c.name)
 def test_deterministic_mode(case):
     """FA_DQ_DETERMINISTIC: parity with the oracle, and dQ bitwise identical
-    across runs (partials are added in a fixed order)."""
+    across runs (every dQ row is summed by one CTA in a fixed key-block
+    order).  dK and dV come from the same key-block sweep as in the atomic
+    mode, so they carry the same bits there."""
     import attention_backward_sm_gb300 as fab
     prep = Prepared(case)
     first = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
@@ -138,6 +139,8 @@ def test_deterministic_mode(case):
         again = prep.run(dq_mode=fab.FA_DQ_DETERMINISTIC)
         for a, b in zip(first, again):
             assert torch.equal(a, b)
+    anyorder = prep.run(dq_mode=fab.FA_DQ_ATOMIC)
+    assert torch.equal(first[1], anyorder[1]) and torch.equal(first[2], anyorder[2])
 
 
 def test_deterministic_full_size_cfg3_causal_bitwise():
@@ -154,8 +157,8 @@ def test_deterministic_full_size_cfg3_causal_bitwise():
 
 
 def test_deterministic_full_size_noncausal_bitwise():
-    """Full-size batch without a mask (rotated sweep order) in deterministic
-    mode: two runs agree bit for bit and the sampled heads match the oracle."""
+    """Full-size batch without a mask in deterministic mode: two runs agree
+    bit for bit and the sampled heads match the oracle."""
     import attention_backward_sm_gb300 as fab
     case = si.cfg3(False)
     subset = sampled(case, 2, seed=8)
@@ -168,8 +171,8 @@ def test_deterministic_full_size_noncausal_bitwise():
 
 def test_deterministic_full_size_cross_bitwise():
     """Cross attention with unequal query and key block counts per sequence
-    (cfg5's lengths; partials added in ascending key-block order): two
-    deterministic runs agree bit for bit and sampled heads match the oracle."""
+    (cfg5's lengths): two deterministic runs agree bit for bit and sampled
+    heads match the oracle."""
     import attention_backward_sm_gb300 as fab
     case = si.cfg5()
     subset = sampled(case, 2, seed=9)
@@ -183,10 +186,10 @@ def test_deterministic_full_size_cross_bitwise():
 
 def test_deterministic_unit_larger_than_the_ring_bound():
     """160 key blocks per (sequence, head), more than the GPU holds CTAs at
-    once: the rotated order (which waits on later-launched blocks) would stall
-    here, so such units take the ascending order.  Properties that hold at any
-    size: bitwise repeats, agreement with the any-order mode up to fp32
-    summation order, and sum_j dV_j = sum_i dO_i."""
+    once (no CTA of the deterministic mode waits on another, so the unit
+    size is free).  Properties that hold at any size: bitwise repeats,
+    agreement with the any-order mode up to fp32 summation order, and
+    sum_j dV_j = sum_i dO_i."""
     import attention_backward_sm_gb300 as fab
     case = si.fixed("det_ring_d64_s20480", 1, 2, 64, 20480, 20480, False, 55)
     q, k, v, do = (t.cuda() for t in case.tensors())
