@@ -56,14 +56,13 @@ constexpr uint32_t COL_S = 0;
 constexpr uint32_t COL_DP0 = 128;       // two dP buffers: [128, 256) and [256, 384)
 constexpr uint32_t COL_ACC = 384;       // dQ accumulator, d columns
 constexpr int KS = 3;                   // K stages
-
 template <int D>
 constexpr int kVStages = (D == 64) ? 3 : 2;
 
 enum {
   B_Q_FULL = 0, B_Q_READY,
-  B_K_FULL0, B_K_READY0 = B_K_FULL0 + KS, B_K_EMPTY0 = B_K_READY0 + KS,
-  B_V_FULL0 = B_K_EMPTY0 + KS, B_V_EMPTY0 = B_V_FULL0 + 3,
+  B_K_FULL0, B_K_READY0 = B_K_FULL0 + 3, B_K_EMPTY0 = B_K_READY0 + 3,   // up to 3 K stages
+  B_V_FULL0 = B_K_EMPTY0 + 3, B_V_EMPTY0 = B_V_FULL0 + 3,
   B_S_FULL = B_V_EMPTY0 + 3, B_P_DONE, B_DP_FULL0, B_DP_FULL1, B_DS_READY, B_DQ_DONE0, B_DQ_DONE1, B_ACC_FULL,
   B_TEARDOWN, NUM_BARS
 };
@@ -100,6 +99,9 @@ __device__ __forceinline__ void mmas_kk(uint32_t d, uint32_t a_tile, uint32_t b_
 }
 // acc (+)= dS K: A (dS, bf16 pairs) from TMEM, K step t at column
 // 64*(t/4) + 8*(t%4); B = K tile read MN-major (head dims contiguous).
+// (dS staged in shared memory instead, so that both operands come from
+// there, measured slower: the softmax then waits for the previous product
+// to have read the single buffer.)
 __device__ __forceinline__ void mmas_dq(uint32_t d, uint32_t a_tmem, uint32_t k_tile, uint32_t idesc, uint32_t acc) {
   const uint64_t b0 = desc_mnmajor(k_tile, 0);
 #pragma unroll 4
@@ -321,6 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
       }
       __syncwarp();
     };
+    // Issue order per key block j: S_{j+1} as soon as the softmax has read
+    // S_j, then dP_{j+1} (its buffer held dS_{j-1}, long consumed), then
+    // acc += dS_j K_j once dS_j is written.  The softmax needs S_{j+1} right
+    // after dS_j and dP_{j+1} right after P_{j+1}, so both are queued on the
+    // tensor pipe ahead of the dQ product, which nothing waits for.
     bool ok = mbar_wait(bar(B_Q_READY), 0, abort, status) && mbar_wait(bar(B_K_READY0), 0, abort, status);
     if (ok) {
       tc_fence_after();
@@ -329,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         mma_commit(bar(B_S_FULL));
       }
       __syncwarp();
-    }
-    for (int j = 0; ok && j < 2 && j < n; ++j) {
-      if (!mbar_wait(bar(B_V_FULL0 + j % VS), (j / VS) & 1, abort, status)) { ok = false; break; }
-      tc_fence_after();
-      issue_dp(j);
+      ok = mbar_wait(bar(B_V_FULL0), 0, abort, status);
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+      }
     }
     for (int j = 0; ok && j < n; ++j) {
       if (j + 1 < n) {
@@ -347,6 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
           mma_commit(bar(B_S_FULL));
         }
         __syncwarp();
+        // dP_{j+1} into buffer (j+1) & 1 once acc += dS_{j-1} K_{j-1} has read it
+        if ((j >= 1 && !mbar_wait(bar(B_DQ_DONE0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, status)) ||
+            !mbar_wait(bar(B_V_FULL0 + (j + 1) % VS), ((j + 1) / VS) & 1, abort, status)) { ok = false; break; }
+        tc_fence_after();
+        issue_dp(j + 1);
       }
       // acc += dS_j K_j, dS_j read from dP buffer j & 1
       if (!mbar_wait(bar(B_DS_READY), j & 1, abort, status)) { ok = false; break; }
@@ -358,13 +370,6 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         mma_commit(bar(B_K_EMPTY0 + sk));    // the dQ product was K_j's last use
       }
       __syncwarp();
-      if (j + 2 < n) {
-        // dP_{j+2} reuses buffer j & 1 once the MMA above has read dS_j
-        if (!mbar_wait(bar(B_DQ_DONE0 + (j & 1)), (j >> 1) & 1, abort, status) ||
-            !mbar_wait(bar(B_V_FULL0 + (j + 2) % VS), ((j + 2) / VS) & 1, abort, status)) { ok = false; break; }
-        tc_fence_after();
-        issue_dp(j + 2);
-      }
     }
     ok = __all_sync(0xffffffffu, ok);
     if (elect_one()) mma_commit(bar(ok ? B_ACC_FULL : B_TEARDOWN));
