@@ -286,8 +286,8 @@ size_t fa_bwd_workspace_size(const int32_t* cu_q_host, const int32_t* cu_kv_host
   for (int b = 0; b < batch; ++b) max_q = cu_q_host[b + 1] - cu_q_host[b] > max_q ? cu_q_host[b + 1] - cu_q_host[b] : max_q;
   ok();
   // head_dim 256: one int32 counter per (batch, head, 64-row query block,
-  // head-dim half, 32-dim quarter), rounded to 256 B
-  const size_t n = static_cast<size_t>(batch) * heads * ((max_q + 63) / 64) * 8;
+  // head-dim half, 32-dim quarter) and the work-item counter, rounded to 256 B
+  const size_t n = static_cast<size_t>(batch) * heads * ((max_q + 63) / 64) * 8 + 1;
   return ((n * 4 + 255) / 256) * 256;
 }
 
@@ -376,6 +376,8 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.tickets = static_cast<int*>(workspace);
+  if (head_dim == 256 && dq_mode == FA_DQ_DETERMINISTIC)
+    p.work_counter = p.tickets + static_cast<size_t>(batch) * heads * ((max_q + 63) / 64) * 8;
   if (need > 0) {
     cudaError_t e = fa::launch_zero_fill(workspace, static_cast<long long>(need), s);
     if (e != cudaSuccess) return cuda_fail(e, "ticket reset");

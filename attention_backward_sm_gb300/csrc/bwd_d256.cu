@@ -143,13 +143,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
   // key/value head, 2 x sequence + head-dimension half).  head_chunk > 1:
   // (sequence, key/value head) units in chunks, key block slow within a
   // chunk, the two head-dimension halves of a key block side by side.
+  //
+  // Deterministic mode (unchunked): a CTA's dQ additions wait for those of
+  // the key blocks before it in the order of the tickets, which are the
+  // CTAs before it in this launch order.  So that every CTA waited for has
+  // certainly started, whatever order the hardware starts CTAs in, the
+  // position in the launch order is taken from a global counter when the CTA
+  // starts instead of from its block index.
   int kvb, hk, b, c;                                 // c: head-dimension half
   if constexpr (!kChunked) {
-    kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                       : static_cast<int>(blockIdx.x);
-    hk = blockIdx.y;
-    b = blockIdx.z >> 1;
-    c = blockIdx.z & 1;
+    int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z;
+    if (p.work_counter != nullptr) {
+      int* item_slot = reinterpret_cast<int*>(smem + Layout::MISC + 8);
+      if (threadIdx.x == 0) *item_slot = atomicAdd(p.work_counter, 1);
+      __syncthreads();
+      const int item = *item_slot;
+      bx = item % static_cast<int>(gridDim.x);
+      by = (item / static_cast<int>(gridDim.x)) % static_cast<int>(gridDim.y);
+      bz = item / static_cast<int>(gridDim.x * gridDim.y);
+    }
+    kvb = p.kv_reverse ? static_cast<int>(gridDim.x) - 1 - bx : bx;
+    hk = by;
+    b = bz >> 1;
+    c = bz & 1;
   } else {
     const int lin = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
     const int units = p.heads_kv * p.batch;

@@ -29,6 +29,8 @@ struct BwdParams {
   const int32_t* cu_kv;
   int* tickets;        // deterministic mode at head_dim 256: one counter per (batch, head, 64-row query
                        // block, head-dim half, 32-dim quarter)
+  int* work_counter;   // deterministic mode at head_dim 256: CTAs take their work items from it in the
+                       // order they start
   int heads;           // query heads
   int heads_kv;        // key/value heads (heads is a multiple of it)
   int causal;          // 1: causal mask (top-left unless bottom_right)
