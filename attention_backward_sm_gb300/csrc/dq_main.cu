@@ -128,6 +128,64 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first, int lane) {
   }
 }
 
+// P phase of one softmax thread: query row r, this warpgroup's 64 key
+// columns of S in TMEM (taddr = the row's lane, first column).  P =
+// 2^(S*scale*log2e - lse2) (= exp(S*scale - m) / l); with MASK, entries
+// outside the row's visible run of key columns [c_lo, c_lo + span) are 0.
+// MASK is a template parameter so that full blocks run a loop without any
+// per-element mask work.
+template <bool MASK>
+__device__ __forceinline__ void softmax_p(uint32_t taddr, float sl2, float neg_lse2, float (&P)[64], int kc0, int c_lo,
+                                          int span) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v[32];
+    tmem_ld32(taddr + half * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c2 = 0; c2 < 16; ++c2) {
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * c2]), __uint_as_float(v[2 * c2 + 1])),
+                                  make_float2(sl2, sl2), make_float2(neg_lse2, neg_lse2));
+      float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+      if (MASK) {
+        const int col = kc0 + half * 32 + 2 * c2;
+        p0 = (static_cast<unsigned>(col - c_lo) < static_cast<unsigned>(span)) ? p0 : 0.f;
+        p1 = (static_cast<unsigned>(col + 1 - c_lo) < static_cast<unsigned>(span)) ? p1 : 0.f;
+      }
+      P[half * 32 + 2 * c2] = p0;
+      P[half * 32 + 2 * c2 + 1] = p1;
+    }
+  }
+}
+
+// dS phase: dS = P * (dP - D) from dP in TMEM (taddr), rounded to bf16 and
+// stored as pairs into the first 32 of the 64 columns just read.
+template <bool MASK>
+__device__ __forceinline__ void softmax_ds(uint32_t taddr, float neg_D, const float (&P)[64]) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v[32];
+    tmem_ld32(taddr + half * 32, v);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int c2 = 0; c2 < 16; ++c2) {
+      const int c0 = half * 32 + 2 * c2;
+      // dS = P * (dP - D), two at a time (packed fp32 add and multiply)
+      float2 ds = __fmul2_rn(make_float2(P[c0], P[c0 + 1]),
+                             __fadd2_rn(make_float2(__uint_as_float(v[2 * c2]), __uint_as_float(v[2 * c2 + 1])),
+                                        make_float2(neg_D, neg_D)));
+      if (MASK) {   // P is 0 where masked, but dP there may be anything (NaN padding)
+        ds.x = (P[c0] != 0.f) ? ds.x : 0.f;
+        ds.y = (P[c0 + 1] != 0.f) ? ds.y : 0.f;
+      }
+      pk[c2] = pack_bf16x2(ds.x, ds.y);
+    }
+    // the first 16 (then 32) columns of this half were already read
+    tmem_st16(taddr + half * 16, pk);
+  }
+}
+
 __device__ __forceinline__ int floordiv(long long a, int b) {
   long long q = a / b;
   if ((a % b) != 0 && a < 0) --q;
@@ -414,52 +472,19 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
       tc_fence_after();
       float P[64];
       const uint32_t t_s = tmem + lane_addr + COL_S + wg * 64;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_ld32(t_s + half * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[2 * c2]), __uint_as_float(v[2 * c2 + 1])),
-                                      make_float2(sl2, sl2), make_float2(neg_lse2, neg_lse2));
-          const int col = wg * 64 + half * 32 + 2 * c2;
-          float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          if (need_mask) {
-            p0 = (static_cast<unsigned>(col - c_lo) < static_cast<unsigned>(span)) ? p0 : 0.f;
-            p1 = (static_cast<unsigned>(col + 1 - c_lo) < static_cast<unsigned>(span)) ? p1 : 0.f;
-          }
-          P[half * 32 + 2 * c2] = p0;
-          P[half * 32 + 2 * c2 + 1] = p1;
-        }
-      }
+      if (need_mask)
+        softmax_p<true>(t_s, sl2, neg_lse2, P, wg * 64, c_lo, span);
+      else
+        softmax_p<false>(t_s, sl2, neg_lse2, P, wg * 64, c_lo, span);
       tc_fence_before();
       mbar_arrive(bar(B_P_DONE));                  // S may be overwritten
       if (!mbar_wait(bar(B_DP_FULL0 + (j & 1)), (j >> 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t t_dp = tmem + lane_addr + COL_DP0 + (j & 1) * 128 + wg * 64;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_ld32(t_dp + half * 32, v);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          const int c0 = half * 32 + 2 * c2;
-          // dS = P * (dP - D), two at a time (packed fp32 add and multiply)
-          float2 ds = __fmul2_rn(make_float2(P[c0], P[c0 + 1]),
-                                 __fadd2_rn(make_float2(__uint_as_float(v[2 * c2]), __uint_as_float(v[2 * c2 + 1])),
-                                            make_float2(neg_D, neg_D)));
-          if (need_mask) {   // P is 0 where masked, but dP there may be anything (NaN padding)
-            ds.x = (P[c0] != 0.f) ? ds.x : 0.f;
-            ds.y = (P[c0 + 1] != 0.f) ? ds.y : 0.f;
-          }
-          pk[c2] = pack_bf16x2(ds.x, ds.y);
-        }
-        // into the first 32 of this warpgroup's 64 columns (already read)
-        tmem_st16(t_dp + half * 16, pk);
-      }
+      if (need_mask)
+        softmax_ds<true>(t_dp, neg_D, P);
+      else
+        softmax_ds<false>(t_dp, neg_D, P);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_DS_READY));
