@@ -65,9 +65,12 @@ enum fa_status {
 
 enum fa_dq_mode {
     FA_DQ_ATOMIC = 0,         /* dQ partials added with fp32 atomics, in any order */
-    FA_DQ_DETERMINISTIC = 1   /* dQ partials added in a fixed key-block order: bitwise reproducible;
-                                 needs fa_bwd_workspace_size() bytes of workspace (one int32 counter
-                                 per batch x head x 128-row query block x 32-row quarter) */
+    FA_DQ_DETERMINISTIC = 1   /* bitwise reproducible dQ.  head_dim 64 / 128: the key-block-outer
+                                 kernel computes dK and dV only, and a query-block-outer kernel sums
+                                 each row of dQ in one CTA in ascending key-block order (no atomics,
+                                 no waits between CTAs, no workspace).  head_dim 256: dQ partials
+                                 added in a fixed key-block order through counters in
+                                 fa_bwd_workspace_size() bytes of workspace */
 };
 
 /* Masks of the _ex entry points (local indices i of the query, j of the key
@@ -207,7 +210,9 @@ int fa_bwd_gqa(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf
  * dimension; each computes the full scores and dP and its half of dK, dV
  * and dQ, over 64-row query blocks.  In FA_DQ_DETERMINISTIC mode the
  * workspace then holds one counter per (batch, head, 64-row query block,
- * head-dim half, 32-dim quarter); fa_bwd_workspace_size accounts for it. */
+ * head-dim half, 32-dim quarter) and one work-item counter from which the
+ * CTAs take their order as they start; fa_bwd_workspace_size accounts for
+ * both. */
 int fa_bwd_ex(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16* dout,
               const float* m, const float* l, const float* D,
               float* dq_acc, fa_bf16* dk, fa_bf16* dv,
