@@ -34,6 +34,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "sm103.cuh"
 
@@ -561,20 +563,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         tmem_ld32(tmem + lane_addr + COL_S + qc0, v);
         tmem_ld_wait();
         uint32_t pk[16];
+        // masked and unmasked blocks as separate instantiations: no
+        // per-element mask work where every column is visible
+        auto p_loop = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float la[4] = {lv[c4].x, lv[c4].y, lv[c4].z, lv[c4].w};
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float la[4] = {lv[c4].x, lv[c4].y, lv[c4].z, lv[c4].w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = c4 * 4 + e;
-            float pv = ex2_approx(fmaf(__uint_as_float(v[col]), sl2, -la[e]));
-            if (need_mask) {
-              const bool vis = static_cast<unsigned>(qc0 + col - c_lo) < static_cast<unsigned>(span);
-              pv = vis ? pv : 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const int col = c4 * 4 + e;
+              float pv = ex2_approx(fmaf(__uint_as_float(v[col]), sl2, -la[e]));
+              if (MASK) {
+                const bool vis = static_cast<unsigned>(qc0 + col - c_lo) < static_cast<unsigned>(span);
+                pv = vis ? pv : 0.f;
+              }
+              P[col] = pv;
             }
-            P[col] = pv;
           }
-        }
+        };
+        if (need_mask)
+          p_loop(std::true_type{});
+        else
+          p_loop(std::false_type{});
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(P[2 * j], P[2 * j + 1]);
         tmem_st16(tmem + lane_addr + COL_S + qc0, pk);
@@ -594,19 +605,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         tmem_ld32(tmem + lane_addr + COL_DP + qc0, v);
         tmem_ld_wait();
         uint32_t pk[16];
+        auto ds_loop = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float da[4] = {dv[c4].x, dv[c4].y, dv[c4].z, dv[c4].w};
-          float ds[4];
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float da[4] = {dv[c4].x, dv[c4].y, dv[c4].z, dv[c4].w};
+            float ds[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = c4 * 4 + e;
-            ds[e] = P[col] * (__uint_as_float(v[col]) - da[e]);
-            if (need_mask) ds[e] = (P[col] != 0.f) ? ds[e] : 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const int col = c4 * 4 + e;
+              ds[e] = P[col] * (__uint_as_float(v[col]) - da[e]);
+              if (MASK) ds[e] = (P[col] != 0.f) ? ds[e] : 0.f;   // dP may hold garbage where masked
+            }
+            pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+            pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
           }
-          pk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-          pk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
+        };
+        if (need_mask)
+          ds_loop(std::true_type{});
+        else
+          ds_loop(std::false_type{});
         const uint32_t ds_row = sbase + L::DS + r * 128;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
