@@ -71,29 +71,38 @@ def peaks():
         return 1900.0, 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ("bwd_main.cu", "bwd_d256.cu", "sm103.cuh", "api.cu", "internal.h")
+COMMON_SOURCES = ("sm103.cuh", "api.cu", "internal.h")
 
 
-def kernel_source_hash():
-    """Hash of every source that decides what a backward launch does (the
-    kernels, their PTX wrappers, the launch order and grid set-up)."""
+def kernel_sources(head_dim: int, dq_mode: int):
+    """The sources that decide what fa_bwd launches for this head_dim and
+    dQ mode: the kernels, their PTX wrappers, the grid set-up and launch
+    order."""
+    if head_dim == 256:
+        return ("bwd_d256.cu",) + COMMON_SOURCES
+    return ("bwd_main.cu",) + (("dq_main.cu",) if dq_mode else ()) + COMMON_SOURCES
+
+
+def kernel_source_hash(head_dim: int = 128, dq_mode: int = 0):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in kernel_sources(head_dim, dq_mode):
         with open(os.path.join(ROOT, "attention_backward_sm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per fa_bwd launch from the committed ncu summary, if it was
-    taken on the current kernel source; otherwise None."""
-    path = os.path.join(ROOT, "profiles", f"fa_bwd_{workload}.md")
+def profiled_traffic(workload: str, head_dim: int, dq_mode: int):
+    """DRAM bytes per fa_bwd call (all its kernels) from the committed ncu
+    summary of this workload and dQ mode, if it was taken on the current
+    sources; otherwise None."""
+    name = f"fa_bwd_det_{workload}.md" if dq_mode else f"fa_bwd_{workload}.md"
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
     mh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not mh or not mt or mh.group(1) != kernel_source_hash():
+    if not mh or not mt or mh.group(1) != kernel_source_hash(head_dim, dq_mode):
         return None
     return float(mt.group(1))
 
@@ -565,13 +574,14 @@ def run_gpu(args):
 
     peak, hbm, peak_src = peaks()
     achieved = flops / (bwd_ms * 1e-3) / 1e12
-    traffic = None if lse_stats else profiled_traffic(args.workload)
+    traffic = None if lse_stats else profiled_traffic(args.workload, case.head_dim, args.dq_mode)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "hbm_gbs": None if traffic is None else traffic / (bwd_ms * 1e-3) / 1e9,
                 "hbm_frac": None if traffic is None else traffic / (bwd_ms * 1e-3) / 1e9 / hbm,
-                "kernel": "fa_bwd (bwd_kernel<%d>)" % case.head_dim if case.head_dim != 256
-                else "fa_bwd (bwd256_kernel)",
+                "kernel": ("fa_bwd (bwd256_kernel)" if case.head_dim == 256 else
+                           "fa_bwd (bwd_kernel<%d> + dq_kernel<%d>)" % (case.head_dim, case.head_dim)
+                           if args.dq_mode else "fa_bwd (bwd_kernel<%d>)" % case.head_dim),
                 "fa_bwd_ms": bwd_ms, "fa_bwd_ms_mean": bwd_mean_ms, "launches_timed": len(bwd_times),
                 "timing": "median of per-launch CUDA events on the launching stream; " +
                 ("the L2-flushed steps" if small else
