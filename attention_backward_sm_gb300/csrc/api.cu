@@ -356,6 +356,8 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
                      "dout", false, q_box)))
     return rc;
   if (max_q > 0 && (rc = make_map(&p.tm_dq, dq_acc, total_q, heads, head_dim, "dq_acc", true))) return rc;
+  if ((rc = make_map(&p.tm_dk, dk, total_kv, heads_kv, head_dim, "dk"))) return rc;
+  if ((rc = make_map(&p.tm_dv, dv, total_kv, heads_kv, head_dim, "dv"))) return rc;
   p.m = m;
   p.l = l;
   p.D = D;

@@ -19,6 +19,8 @@ struct BwdParams {
   CUtensorMap tm_v;
   CUtensorMap tm_do;  // [total_q rows, H*d cols]
   CUtensorMap tm_dq;  // dq_acc: [total_q rows, H*d cols] fp32, box 32 x 32, 128B swizzle (reduce-add target)
+  CUtensorMap tm_dk;  // dk: [total_kv rows, Hkv*d cols] bf16, box 64 x 128, 128B swizzle (store target)
+  CUtensorMap tm_dv;  // dv: as dk
   const float* m;
   const float* l;
   const float* D;

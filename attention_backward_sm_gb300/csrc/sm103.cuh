@@ -146,6 +146,14 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* desc, uint32_t src
                "r"(src), "r"(x), "r"(y)
                : "memory");
 }
+// 2-D tiled store of one shared-memory box into global memory (rows past
+// the tensor's extent are not written), tracked like the reduce-add.
+__device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(desc)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until the shared-memory sources of every committed bulk group of
 // this thread have been read (the buffer may then be rewritten).
