@@ -33,9 +33,11 @@
 // warps 0-3, 152 for the softmax warpgroups, 152 for the write-back, which
 // holds a whole 128-column dQ partial; the sum is exactly the 65536 the
 // block is launched with):
-//   warp 0      TMA producer: K, V once; Q and per-row stats per block
-//               (2-stage ring); zeroes rows past a sequence end
-//   warp 2      TMA producer of dO (2-stage ring), independent of warp 0
+//   warp 0      TMA producer of K and V (once per CTA)
+//   warp 3      TMA producer of Q and the per-row stats (2- or 3-stage
+//               ring), so that the first Q block loads alongside K and V
+//   warp 2      TMA producer of dO (2-stage ring)
+//               (each producer zeroes tile rows past a sequence end)
 //   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
 //   warps 4-11  two softmax warpgroups, each owning 64 of the 128 query
 //               columns for all 128 key rows; at the end dV (4-7), dK (8-11)
@@ -63,7 +65,7 @@ constexpr int kThreads = 512;
 // Registers per thread: the block launches with 65536 / 512 = 128 and each
 // warpgroup then moves to its own budget.
 constexpr uint32_t kRegLaunch = 65536 / kThreads;
-constexpr uint32_t kRegOther = 56;     // warps 0-3: producers, MMA issuer, one idle warp
+constexpr uint32_t kRegOther = 56;     // warps 0-3: producers and MMA issuer
 constexpr uint32_t kRegSoftmax = 152;  // warps 4-11
 constexpr uint32_t kRegDrain = 152;    // warps 12-15
 static_assert(128 * kRegOther + 256 * kRegSoftmax + 128 * kRegDrain <= 65536, "register budgets exceed the launch");
@@ -425,8 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       __syncwarp();
       // Loads issued but not yet seen complete must land before the CTA
       // exits, even on the abort path: remember their barriers and parities.
-      int pend_kv = 1, pend_q = -1;
-      uint32_t par_q = 0;
+      int pend_kv = 1;
       bool ok = mbar_wait(bar(B_KV_FULL), 0, abort, status);
       if (ok) {
         pend_kv = 0;
@@ -437,74 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_KV_READY));
       }
-      // Raw row statistics (m, l, D) of a block are loaded one block ahead
-      // into registers and only combined (lse2 = m*log2(e) + log2(l)) when
-      // stored, so their latency hides behind the waits of the current block.
-      float rm[4], rl[4], rd[4], nm[4], nl[4], nd[4];
-      auto load_stats = [&](int k, float (&a)[4], float (&b)[4], float (&c)[4]) {
-        const int qb = qb_of(k);
-        const int q_valid = min(BN, s1 - qb * BN);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = lane + 32 * j;
-          a[j] = 0.f;
-          b[j] = 1.f;
-          c[j] = 0.f;
-          if (k < n_it && r < q_valid) {
-            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
-            a[j] = __ldg(p.m + idx);
-            if (!p.stats_lse) b[j] = __ldg(p.l + idx);
-            c[j] = __ldg(p.D + idx);
-          }
-        }
-      };
-      load_stats(0, nm, nl, nd);
-      // Q (with the row statistics) here; dO has a producer warp of its own,
-      // so that each stream's load is issued as soon as its stage is free:
-      // loads share the SM's TMA engine with the dQ reduce-adds and take
-      // over a thousand cycles to land.
-      for (int k = 0; ok && k < n_it; ++k) {
-        const int s = k % NQS;
-        const uint32_t use = k / NQS;               // how often stage s was filled before
-        const uint32_t prev = (use - 1) & 1;        // parity of this stage's previous release
-        const int qb = qb_of(k);
-        const int hq = hq_of(k);
-        const int q_row0 = q_start + qb * BN;
-        const int q_valid = min(BN, s1 - qb * BN);
-        if (k >= NQS && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), L::TILE);
-          for (int c = 0; c < L::NCH; ++c)
-            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, hq * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
-        }
-        pend_q = s;
-        par_q = use & 1;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          rm[j] = nm[j];
-          rl[j] = nl[j];
-          rd[j] = nd[j];
-        }
-        load_stats(k + 1, nm, nl, nd);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // log2 of the softmax denominator, exp(x - m) / l = 2^(x*log2e - lse2)
-          // stored negated: the softmax adds them with packed FMAs / adds
-          st_lse[s * 128 + lane + 32 * j] = -(rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j])));
-          st_D[s * 128 + lane + 32 * j] = -rd[j];
-        }
-        if (!mbar_wait(bar(B_Q_FULL0 + s), use & 1, abort, status)) break;
-        pend_q = -1;
-        if (q_valid < BN) {
-          zero_rows<D>(sbase + L::Q + s * L::TILE, q_valid, lane);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
-      }
       volatile int no_abort = 0;
       if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
-      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ dO producer
@@ -893,7 +828,81 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       if (lane == 0 && issued) bulk_wait_all0();
     }
   } else {
-    setmaxnreg_to<kRegOther, kRegLaunch>();   // warp 3 only waits at the final barrier
+    // ------------------------------------------------------------ Q producer (warp 3)
+    setmaxnreg_to<kRegOther, kRegLaunch>();
+    if (n_it > 0) {
+      // a load issued but not seen complete must land before the CTA exits
+      int pend_q = -1;
+      uint32_t par_q = 0;
+      bool ok = true;
+      // Raw row statistics (m, l, D) of a block are loaded one block ahead
+      // into registers and only combined (lse2 = m*log2(e) + log2(l)) when
+      // stored, so their latency hides behind the waits of the current block.
+      float rm[4], rl[4], rd[4], nm[4], nl[4], nd[4];
+      auto load_stats = [&](int k, float (&a)[4], float (&b)[4], float (&c)[4]) {
+        const int qb = qb_of(k);
+        const int q_valid = min(BN, s1 - qb * BN);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane + 32 * j;
+          a[j] = 0.f;
+          b[j] = 1.f;
+          c[j] = 0.f;
+          if (k < n_it && r < q_valid) {
+            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
+            a[j] = __ldg(p.m + idx);
+            if (!p.stats_lse) b[j] = __ldg(p.l + idx);
+            c[j] = __ldg(p.D + idx);
+          }
+        }
+      };
+      load_stats(0, nm, nl, nd);
+      // Q with the row statistics.  K / V, Q and dO have producer warps of
+      // their own, so that each stream's load is issued as soon as its stage
+      // is free: loads share the SM's TMA engine with the dQ reduce-adds and
+      // take over a thousand cycles to land.
+      for (int k = 0; ok && k < n_it; ++k) {
+        const int s = k % NQS;
+        const uint32_t use = k / NQS;               // how often stage s was filled before
+        const uint32_t prev = (use - 1) & 1;        // parity of this stage's previous release
+        const int qb = qb_of(k);
+        const int hq = hq_of(k);
+        const int q_row0 = q_start + qb * BN;
+        const int q_valid = min(BN, s1 - qb * BN);
+        if (k >= NQS && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), L::TILE);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, hq * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
+        }
+        pend_q = s;
+        par_q = use & 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          rm[j] = nm[j];
+          rl[j] = nl[j];
+          rd[j] = nd[j];
+        }
+        load_stats(k + 1, nm, nl, nd);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // log2 of the softmax denominator, exp(x - m) / l = 2^(x*log2e - lse2)
+          // stored negated: the softmax adds them with packed FMAs / adds
+          st_lse[s * 128 + lane + 32 * j] = -(rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j])));
+          st_D[s * 128 + lane + 32 * j] = -rd[j];
+        }
+        if (!mbar_wait(bar(B_Q_FULL0 + s), use & 1, abort, status)) break;
+        pend_q = -1;
+        if (q_valid < BN) {
+          zero_rows<D>(sbase + L::Q + s * L::TILE, q_valid, lane);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
+      }
+      volatile int no_abort = 0;
+      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
+    }
   }
 
   tc_fence_before();
