@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
                 ok = false;
                 break;
               }
-              __nanosleep(32);
+              // (polled without a sleep: a 32 ns sleep here cost 2.6 %)
             }
           }
           if (!ok) break;

@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                 ok = false;
                 break;
               }
-              __nanosleep(32);
+              // (polled without a sleep: a 32 ns sleep here cost 3 % at d = 64)
             }
           }
           if (!ok) break;
