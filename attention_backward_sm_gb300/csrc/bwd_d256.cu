@@ -26,10 +26,11 @@
 // through the dO stages once on its way to TMEM), dS 16 KB, dQ staging
 // 16 KB, statistics.
 //
-// Warp roles (512 threads): warp 0 TMA producer (K, V, Q, statistics),
-// warp 2 TMA producer of dO, warp 1 TMEM allocator and MMA issuer, warps 4-11 two softmax warpgroups (32 query columns each;
-// warpgroup 0 also moves V into TMEM; at the end dV_c / dK_c), warps 12-15
-// dQ write-back (lane = head dimension).  Every wait is bounded.
+// Warp roles (512 threads): warp 0 TMA producer of K and V, warp 3 of Q and
+// the row statistics, warp 2 of dO, warp 1 TMEM allocator and MMA issuer,
+// warps 4-11 two softmax warpgroups (32 query columns each; warpgroup 0
+// also moves V into TMEM; at the end dV_c / dK_c), warps 12-15 dQ
+// write-back (lane = head dimension).  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ K / V producer
     setmaxnreg_to<kRegOther, kRegLaunch>();
     if (n_it > 0) {
       if (lane == 0) {
@@ -266,8 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         }
       }
       __syncwarp();
-      int pend_kv = 1, pend_q = -1;
-      uint32_t par_q = 0;
+      int pend_kv = 1;
       bool ok = mbar_wait(bar(B_KV_FULL), 0, abort, status);
       if (ok) {
         pend_kv = 0;
@@ -280,65 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_KV_READY));
       }
-      float nm[2], nl[2], nd[2], rm[2], rl[2], rd[2];
-      auto load_stats = [&](int k, float (&a)[2], float (&bb)[2], float (&cc)[2]) {
-        const int qb = qb_of(k);
-        const int q_valid = min(BN, s1 - qb * BN);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int r = lane + 32 * j;
-          a[j] = 0.f;
-          bb[j] = 1.f;
-          cc[j] = 0.f;
-          if (k < n_it && r < q_valid) {
-            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
-            a[j] = __ldg(p.m + idx);
-            if (!p.stats_lse) bb[j] = __ldg(p.l + idx);
-            cc[j] = __ldg(p.D + idx);
-          }
-        }
-      };
-      load_stats(0, nm, nl, nd);
-      for (int k = 0; ok && k < n_it; ++k) {
-        const int s = k & 1;
-        const uint32_t prev = ((k >> 1) - 1) & 1;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          rm[j] = nm[j];
-          rl[j] = nl[j];
-          rd[j] = nd[j];
-        }
-        load_stats(k + 1, nm, nl, nd);
-        const int qb = qb_of(k);
-        const int hq = hq_of(k);
-        const int q_row0 = q_start + qb * BN;
-        const int q_valid = min(BN, s1 - qb * BN);
-        if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), TILE_Q);
-          for (int ch = 0; ch < 4; ++ch)
-            tma_load_2d(sbase + L::Q + s * TILE_Q + ch * CHUNK_Q, &p.tm_q, hq * D + ch * 64, q_row0,
-                        bar(B_Q_FULL0 + s));
-        }
-        pend_q = s;
-        par_q = (k >> 1) & 1;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          st_lse[s * BN + lane + 32 * j] = rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j]));
-          st_D[s * BN + lane + 32 * j] = rd[j];
-        }
-        if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;
-        pend_q = -1;
-        if (q_valid < BN) {
-          zero_rows(sbase + L::Q + s * TILE_Q, q_valid, BN, CHUNK_Q, lane);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
-      }
       volatile int no_abort = 0;
       if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
-      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ dO producer
@@ -729,7 +672,73 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
     }
     if (lane == 0 && issued) bulk_wait_all0();
   } else {
+    // ------------------------------------------------------------ Q producer (warp 3)
+    // (its own warp, so that the first Q block loads alongside K and V)
     setmaxnreg_to<kRegOther, kRegLaunch>();
+    if (n_it > 0) {
+      // a load issued but not seen complete must land before the CTA exits
+      int pend_q = -1;
+      uint32_t par_q = 0;
+      bool ok = true;
+      float nm[2], nl[2], nd[2], rm[2], rl[2], rd[2];
+      auto load_stats = [&](int k, float (&a)[2], float (&bb)[2], float (&cc)[2]) {
+        const int qb = qb_of(k);
+        const int q_valid = min(BN, s1 - qb * BN);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int r = lane + 32 * j;
+          a[j] = 0.f;
+          bb[j] = 1.f;
+          cc[j] = 0.f;
+          if (k < n_it && r < q_valid) {
+            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
+            a[j] = __ldg(p.m + idx);
+            if (!p.stats_lse) bb[j] = __ldg(p.l + idx);
+            cc[j] = __ldg(p.D + idx);
+          }
+        }
+      };
+      load_stats(0, nm, nl, nd);
+      for (int k = 0; ok && k < n_it; ++k) {
+        const int s = k & 1;
+        const uint32_t prev = ((k >> 1) - 1) & 1;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          rm[j] = nm[j];
+          rl[j] = nl[j];
+          rd[j] = nd[j];
+        }
+        load_stats(k + 1, nm, nl, nd);
+        const int qb = qb_of(k);
+        const int hq = hq_of(k);
+        const int q_row0 = q_start + qb * BN;
+        const int q_valid = min(BN, s1 - qb * BN);
+        if (k >= 2 && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), TILE_Q);
+          for (int ch = 0; ch < 4; ++ch)
+            tma_load_2d(sbase + L::Q + s * TILE_Q + ch * CHUNK_Q, &p.tm_q, hq * D + ch * 64, q_row0,
+                        bar(B_Q_FULL0 + s));
+        }
+        pend_q = s;
+        par_q = (k >> 1) & 1;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          st_lse[s * BN + lane + 32 * j] = rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j]));
+          st_D[s * BN + lane + 32 * j] = rd[j];
+        }
+        if (!mbar_wait(bar(B_Q_FULL0 + s), (k >> 1) & 1, abort, status)) break;
+        pend_q = -1;
+        if (q_valid < BN) {
+          zero_rows(sbase + L::Q + s * TILE_Q, q_valid, BN, CHUNK_Q, lane);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_Q_READY0 + s));
+      }
+      volatile int no_abort = 0;
+      if (pend_q >= 0) mbar_wait(bar(B_Q_FULL0 + pend_q), par_q, &no_abort, status);
+    }
   }
 
   tc_fence_before();
