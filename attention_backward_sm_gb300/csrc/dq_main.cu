@@ -493,15 +493,44 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
     // Warpgroup g stores head dims [g D/2, (g+1) D/2) of its rows.
     if (__all_sync(0xffffffffu, ok && mbar_wait(bar(B_ACC_FULL), 0, abort, status))) {
       tc_fence_after();
-      float* dst = p.dq_acc + (q_start + qb * BQ + r) * rs + h * D + wg * (D / 2);
+      if (q_valid == BQ) {
+        // A whole query block: each warp stages its 32 rows x D/2 columns as
+        // 128B-swizzled [32 x 32] fp32 boxes in the Q / dO tiles, which no
+        // MMA reads any more, and stores them with TMA (coalesced, instead of
+        // 16-byte pieces of 32 rows per warp store).  A partial block is
+        // written per row below, so that no row of the next sequence is
+        // touched.
+        const uint32_t box0 = sbase + L::Q + (wg * 4 + quarter) * (D / 64) * 4096;
 #pragma unroll
-      for (int ch = 0; ch < D / 64; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_addr + COL_ACC + wg * (D / 2) + ch * 32, v);
-        tmem_ld_wait();
-        if (r < q_valid) {
+        for (int ch = 0; ch < D / 64; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + COL_ACC + wg * (D / 2) + ch * 32, v);
+          tmem_ld_wait();
+          const uint32_t row = box0 + ch * 4096 + lane * 128;
 #pragma unroll
-          for (int g = 0; g < 8; ++g) st_global_v4(dst + ch * 32 + g * 4, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          for (int g = 0; g < 8; ++g)
+            st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int ch = 0; ch < D / 64; ++ch)
+            tma_store_2d(&p.tm_dq, box0 + ch * 4096, h * D + wg * (D / 2) + ch * 32, q_start + qb * BQ + quarter * 32);
+          bulk_commit();
+          bulk_wait_read0();   // the boxes are read before the CTA exits
+        }
+        __syncwarp();
+      } else {
+        float* dst = p.dq_acc + (q_start + qb * BQ + r) * rs + h * D + wg * (D / 2);
+#pragma unroll
+        for (int ch = 0; ch < D / 64; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + COL_ACC + wg * (D / 2) + ch * 32, v);
+          tmem_ld_wait();
+          if (r < q_valid) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) st_global_v4(dst + ch * 32 + g * 4, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          }
         }
       }
     }
