@@ -72,7 +72,7 @@ enum {
   B_Q_FULL0, B_Q_FULL1, B_Q_READY0, B_Q_READY1, B_Q_EMPTY0, B_Q_EMPTY1,
   B_DO_FULL0, B_DO_FULL1, B_DO_READY0, B_DO_READY1, B_DO_EMPTY0, B_DO_EMPTY1,
   B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
-  B_TEARDOWN, NUM_BARS
+  B_TEARDOWN, B_EPI0, B_EPI1, NUM_BARS
 };
 
 struct Layout {
@@ -240,6 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
     mbar_init(bar(B_DQ_EMPTY), 128);
     mbar_init(bar(B_ACC_FULL), 1);
     mbar_init(bar(B_TEARDOWN), 1);
+    mbar_init(bar(B_EPI0), 128);   // dV_c / dK_c tile staged by its warpgroup
+    mbar_init(bar(B_EPI1), 128);
     mbar_init_fence();
   }
   if (warp == 1) {
@@ -590,19 +592,53 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
     } else if (__all_sync(0xffffffffu, ok && mbar_wait(bar(B_ACC_FULL), 0, abort, status))) {
       tc_fence_after();
       const uint32_t col0 = (wg == 0) ? COL_DV : COL_DK;
+      if (kv_valid == BM) {
+        // A whole key block: dV_c (warpgroup 0) / dK_c (1) staged as bf16 in
+        // two 64-column chunks of the K tile, which no MMA reads any more,
+        // and written by TMA; a partial block is written per row below, so
+        // that no row of the next sequence is touched.
+        const uint32_t tile = sbase + L::K + wg * 2 * CHUNK_K;
+        const uint32_t row = tile + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll 1
-      for (int ch = 0; ch < HALF / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_addr + col0 + ch * 32, v);
-        tmem_ld_wait();
-        if (r < kv_valid) {
+        for (int ch = 0; ch < HALF / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + col0 + ch * 32, v);
+          tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               w[e] = pack_bf16x2(mul * __uint_as_float(v[g * 8 + 2 * e]), mul * __uint_as_float(v[g * 8 + 2 * e + 1]));
-            st_global_v4(dst + (ch * 32 + g * 8) * 2, w[0], w[1], w[2], w[3]);
+            const int u = (ch & 1) * 4 + g;   // 16-byte unit within the 128-byte row of a 64-column chunk
+            st_shared_v4(row + (ch >> 1) * CHUNK_K + ((u ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_EPI0 + wg));
+        // One thread per warpgroup waits (bounded) for the other 127 rows.
+        if (quarter == 0 && lane == 0 && mbar_wait(bar(B_EPI0 + wg), 0, abort, status)) {
+          for (int cc = 0; cc < 2; ++cc)
+            tma_store_2d((wg == 0) ? &p.tm_dv : &p.tm_dk, tile + cc * CHUNK_K, hk * D + c * HALF + cc * 64,
+                         kv_start + kvb * BM);
+          bulk_commit();
+          bulk_wait_read0();   // the tile is read before the CTA exits
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < HALF / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + col0 + ch * 32, v);
+          tmem_ld_wait();
+          if (r < kv_valid) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(mul * __uint_as_float(v[g * 8 + 2 * e]), mul * __uint_as_float(v[g * 8 + 2 * e + 1]));
+              st_global_v4(dst + (ch * 32 + g * 8) * 2, w[0], w[1], w[2], w[3]);
+            }
           }
         }
       }
