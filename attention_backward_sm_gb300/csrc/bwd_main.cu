@@ -41,9 +41,11 @@
 //   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
 //   warps 4-11  two softmax warpgroups, each owning 64 of the 128 query
 //               columns for all 128 key rows; at the end dV (4-7), dK (8-11)
-//   warps 12-15 dQ write-back: TMEM -> shared memory (buffers the MMAs are
-//               done with: the block's dO and Q (d = 128) or dS (d = 64)
-//               buffers) -> TMA reduce-add
+//   warps 12-15 dQ write-back: TMEM -> shared memory (d = 128: the block's
+//               Q and dO buffers, which the MMAs are done with; d = 64: a
+//               staging area of its own) -> TMA reduce-add
+// The dK / dV epilogue of a whole key block at d = 128 goes through the dead
+// K / V tiles and TMA stores; otherwise each thread stores its own row.
 // Every mbarrier wait is bounded (see sm103.cuh); on a timeout the CTA
 // records FA_ERR_TIMEOUT in the status word, drains and frees TMEM.
 #include <cuda.h>
