@@ -36,6 +36,8 @@
 //   warp 0      TMA producer of K and V (once per CTA)
 //   warp 3      TMA producer of Q and the per-row stats (2- or 3-stage
 //               ring), so that the first Q block loads alongside K and V
+//               (d = 128 without a mask: from the third block on, the Q
+//               load itself is issued by write-back warp 12, see below)
 //   warp 2      TMA producer of dO (2-stage ring)
 //               (each producer zeroes tile rows past a sequence end)
 //   warp 1      TMEM allocator and MMA issuer (one elected lane issues)
@@ -86,7 +88,7 @@ enum {
   B_DO_FULL0 = B_Q_EMPTY0 + 3,
   B_DO_FULL1, B_DO_READY0, B_DO_READY1, B_DO_EMPTY0, B_DO_EMPTY1,
   B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
-  B_TEARDOWN, B_EPI0, B_EPI1, NUM_BARS
+  B_TEARDOWN, B_EPI0, B_EPI1, B_Q_ISSUED, NUM_BARS
 };
 
 // Where a dQ partial lives on its way to TMA.  d = 128: tensor memory is
@@ -304,6 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   // dP columns, Q and dO buffers free of dQ partials (d = 64 keeps its
   // partial in columns and a staging area of its own)
   constexpr bool kSep = kOwnDQ<D> || !kDQ;
+  // d = 128 with the dQ partial staged in the Q / dO buffers, no mask: the
+  // Q load of block k + NQS is issued by a write-back warp once TMA has read
+  // the half staged in that Q buffer and before the half staged in the dO
+  // buffer is reduce-added, so that it does not queue behind 32 KB of
+  // write-out on the SM's TMA engine (cfg3-nc +0.7 %; under a causal mask
+  // the later release of the dO buffer cost 2 %, so masked sweeps keep the
+  // producer's own order)
+  const bool q_by_drain = kDQ && !kOwnDQ<D> && !p.causal;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
 
@@ -399,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     mbar_init(bar(B_TEARDOWN), 1);
     mbar_init(bar(B_EPI0), 128);   // dV / dK tile staged by its warpgroup
     mbar_init(bar(B_EPI1), 128);
+    mbar_init(bar(B_Q_ISSUED), 1); // (d = 128, atomic) the next Q load is issued
     mbar_init_fence();
   }
   if (warp == 1) {
@@ -762,6 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           st_shared_v4(row + ((g ^ (lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
       };
       bool issued = false;
+      int last_q = -1;   // (warp 12) the last block whose Q load this warp issued
 
       for (int k = 0; k < n_it; ++k) {
         const int s = k & 1;
@@ -810,6 +822,35 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         fence_proxy_async_smem();
         __syncwarp();
+        if (q_by_drain) {
+          // the first half has been read: its Q buffer goes back, and the
+          // Q load of block k + NQS (issued by warp 12 once all four halves
+          // are read) enters the TMA engine ahead of the second half
+          if (lane == 0) {
+            bulk_wait_read0();
+            mbar_arrive(bar(B_Q_EMPTY0 + k % NQS));
+          }
+          __syncwarp();
+          const int kn = k + NQS;
+          if (kn < n_it) {
+            if (quarter == 0) {
+              if (lane == 0) {
+                if (mbar_wait(bar(B_Q_EMPTY0 + k % NQS), (k / NQS) & 1, abort, status)) {
+                  const uint32_t qbuf = sbase + L::Q + (k % NQS) * L::TILE;
+                  mbar_arrive_expect_tx(bar(B_Q_FULL0 + k % NQS), L::TILE);
+                  for (int c = 0; c < L::NCH; ++c)
+                    tma_load_2d(qbuf + c * CHUNK, &p.tm_q, hq_of(kn) * D + c * 64, q_start + qb_of(kn) * BN,
+                                bar(B_Q_FULL0 + k % NQS));
+                  last_q = kn;
+                }
+                mbar_arrive(bar(B_Q_ISSUED));
+              }
+            } else if (!mbar_wait(bar(B_Q_ISSUED), k & 1, abort, status)) {
+              break;
+            }
+            __syncwarp();
+          }
+        }
         if (lane == 0) {
           if (BPH == 2) {
             tma_reduce_add_2d(&p.tm_dq, slot_b, hq * D + 64, y);
@@ -819,8 +860,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           }
           bulk_commit();
           if (!kOwnDQ<D>) {
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
-            mbar_arrive(bar(B_Q_EMPTY0 + k % NQS));
+            if (!q_by_drain) {
+              asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // first half read
+              mbar_arrive(bar(B_Q_EMPTY0 + k % NQS));
+            }
             bulk_wait_read0();                                               // second half read
             mbar_arrive(bar(B_DO_EMPTY0 + s));
           }
@@ -828,6 +871,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         __syncwarp();
       }
       if (lane == 0 && issued) bulk_wait_all0();
+      if (lane == 0 && last_q >= 0) {
+        // Q loads this warp issued land before the CTA exits, also after an
+        // abort (the Q producer then stops waiting for them)
+        volatile int no_abort = 0;
+        for (int b = max(NQS, last_q - NQS + 1); b <= last_q; ++b)
+          mbar_wait(bar(B_Q_FULL0 + b % NQS), (b / NQS) & 1, &no_abort, status);
+      }
     }
   } else {
     // ------------------------------------------------------------ Q producer (warp 3)
@@ -872,13 +922,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         const int q_row0 = q_start + qb * BN;
         const int q_valid = min(BN, s1 - qb * BN);
         if (k >= NQS && !mbar_wait(bar(B_Q_EMPTY0 + s), prev, abort, status)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), L::TILE);
-          for (int c = 0; c < L::NCH; ++c)
-            tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, hq * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
+        if (!q_by_drain || k < NQS) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_Q_FULL0 + s), L::TILE);
+            for (int c = 0; c < L::NCH; ++c)
+              tma_load_2d(sbase + L::Q + s * L::TILE + c * CHUNK, &p.tm_q, hq * D + c * 64, q_row0, bar(B_Q_FULL0 + s));
+          }
+          pend_q = s;
+          par_q = use & 1;
         }
-        pend_q = s;
-        par_q = use & 1;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           rm[j] = nm[j];
