@@ -33,7 +33,8 @@
 // warps 0-3, 152 for the softmax warpgroups, 152 for the write-back, which
 // holds a whole 128-column dQ partial; the sum is exactly the 65536 the
 // block is launched with):
-//   warp 0      TMA producer of K and V (once per CTA)
+//   warp 0      TMA producer of K and V (once per CTA); d = 128 without
+//               the dQ partials: then also of the per-row stats
 //   warp 3      TMA producer of Q and the per-row stats (2- or 3-stage
 //               ring), so that the first Q block loads alongside K and V
 //               (d = 128 without a mask: from the third block on, the Q
@@ -88,7 +89,7 @@ enum {
   B_DO_FULL0 = B_Q_EMPTY0 + 3,
   B_DO_FULL1, B_DO_READY0, B_DO_READY1, B_DO_EMPTY0, B_DO_EMPTY1,
   B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
-  B_TEARDOWN, B_EPI0, B_EPI1, B_Q_ISSUED, NUM_BARS
+  B_TEARDOWN, B_EPI0, B_EPI1, B_Q_ISSUED, B_ST_READY0, B_ST_READY1, B_ST_READY2, NUM_BARS
 };
 
 // Where a dQ partial lives on its way to TMA.  d = 128: tensor memory is
@@ -314,6 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   // the later release of the dO buffer cost 2 %, so masked sweeps keep the
   // producer's own order)
   const bool q_by_drain = kDQ && !kOwnDQ<D> && !p.causal;
+  // d = 128 without the dQ partials (the deterministic mode): the row
+  // statistics come from the K / V producer, idle once K and V have landed,
+  // so that the Q producer issues each Q load without waiting on the
+  // statistics' global loads (cfg3 +2.7 %, cfg3-nc +2.3 %; with the dQ
+  // partials, and at d = 64, the Q producer keeping them measured faster)
+  constexpr bool kStatsW0 = !kDQ && D == 128;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
 
@@ -379,6 +386,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
   auto bar = [&](int i) { return bars + 8u * i; };
   float* st_lse = reinterpret_cast<float*>(smem + L::STATS);          // [kQStages][128]
   float* st_D = reinterpret_cast<float*>(smem + L::STATS_D);          // [kQStages][128]
+  // Raw row statistics (m, l, D) of a block are loaded one block ahead
+  // into registers (lane + 32 j holds row j of the lane) and only combined
+  // (lse2 = m*log2(e) + log2(l)) when stored, so that their latency hides
+  // behind the waits of the current block.
+  auto load_stats = [&](int k, float (&a)[4], float (&b)[4], float (&c)[4]) {
+    const int qb = qb_of(k);
+    const int q_valid = min(BN, s1 - qb * BN);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = lane + 32 * j;
+      a[j] = 0.f;
+      b[j] = 1.f;
+      c[j] = 0.f;
+      if (k < n_it && r < q_valid) {
+        const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
+        a[j] = __ldg(p.m + idx);
+        if (!p.stats_lse) b[j] = __ldg(p.l + idx);
+        c[j] = __ldg(p.D + idx);
+      }
+    }
+  };
+  auto store_stats = [&](int s, const float (&a)[4], const float (&b)[4], const float (&c)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // log2 of the softmax denominator, exp(x - m) / l = 2^(x*log2e - lse2),
+      // stored negated: the softmax adds them with packed FMAs / adds
+      st_lse[s * 128 + lane + 32 * j] = -(a[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(b[j])));
+      st_D[s * 128 + lane + 32 * j] = -c[j];
+    }
+  };
   constexpr int NQS = kQStages<D>;
 
   if (threadIdx.x == 0) {
@@ -388,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     for (int s = 0; s < NQS; ++s) {
       mbar_init(bar(B_Q_FULL0 + s), 1);
       mbar_init(bar(B_Q_READY0 + s), 1);
+      mbar_init(bar(B_ST_READY0 + s), 1);   // (kStatsW0) the stage's row statistics written
       // released by the four write-back warps where they stage a dQ half in
       // it (d = 128), else by the MMA commit after the block's last use
       mbar_init(bar(B_Q_EMPTY0 + s), kSep ? 1 : 4);
@@ -438,6 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
       }
       __syncwarp();
+      // (kStatsW0) the row statistics are loaded here.
+      float rm[4], rl[4], rd[4], nm[4], nl[4], nd[4];
+      if (kStatsW0) load_stats(0, nm, nl, nd);
       // Loads issued but not yet seen complete must land before the CTA
       // exits, even on the abort path: remember their barriers and parities.
       int pend_kv = 1;
@@ -450,6 +491,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_KV_READY));
+      }
+      if (kStatsW0 && ok) {
+        for (int k = 0; k < n_it; ++k) {
+          const int s = k % NQS;
+          // the stage's statistics slot is free once its previous block's dK
+          // has run (the release of its Q buffer)
+          if (k >= NQS && !mbar_wait(bar(B_Q_EMPTY0 + s), ((k / NQS) - 1) & 1, abort, status)) break;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            rm[j] = nm[j];
+            rl[j] = nl[j];
+            rd[j] = nd[j];
+          }
+          load_stats(k + 1, nm, nl, nd);
+          store_stats(s, rm, rl, rd);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_ST_READY0 + s));
+        }
       }
       volatile int no_abort = 0;
       if (pend_kv) mbar_wait(bar(B_KV_FULL), 0, &no_abort, status);
@@ -649,7 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       const int span = (r < kv_valid) ? max(0, c_end - c_lo) : 0;
       const bool need_mask = __any_sync(0xffffffffu, c_lo > wg * 64 || c_lo + span < wg * 64 + 64);
       const int qs = k % NQS;
-      if (!mbar_wait(bar(B_Q_READY0 + qs), (k / NQS) & 1, abort, status)) { ok = false; break; }
+      // the row statistics of this block are in shared memory
+      if (!mbar_wait(bar((kStatsW0 ? B_ST_READY0 : B_Q_READY0) + qs), (k / NQS) & 1, abort, status)) { ok = false; break; }
       // The 64 per-column statistics are read into registers before the
       // scores are waited for: shared-memory loads queue behind the MMAs'
       // operand reads, so their latency is hidden here rather than inside
@@ -887,28 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
       int pend_q = -1;
       uint32_t par_q = 0;
       bool ok = true;
-      // Raw row statistics (m, l, D) of a block are loaded one block ahead
-      // into registers and only combined (lse2 = m*log2(e) + log2(l)) when
-      // stored, so their latency hides behind the waits of the current block.
+      // (unless kStatsW0) the row statistics are loaded here as well
       float rm[4], rl[4], rd[4], nm[4], nl[4], nd[4];
-      auto load_stats = [&](int k, float (&a)[4], float (&b)[4], float (&c)[4]) {
-        const int qb = qb_of(k);
-        const int q_valid = min(BN, s1 - qb * BN);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = lane + 32 * j;
-          a[j] = 0.f;
-          b[j] = 1.f;
-          c[j] = 0.f;
-          if (k < n_it && r < q_valid) {
-            const long long idx = static_cast<long long>(q_start + qb * BN + r) * H + hq_of(k);
-            a[j] = __ldg(p.m + idx);
-            if (!p.stats_lse) b[j] = __ldg(p.l + idx);
-            c[j] = __ldg(p.D + idx);
-          }
-        }
-      };
-      load_stats(0, nm, nl, nd);
+      if (!kStatsW0) load_stats(0, nm, nl, nd);
       // Q with the row statistics.  K / V, Q and dO have producer warps of
       // their own, so that each stream's load is issued as soon as its stage
       // is free: loads share the SM's TMA engine with the dQ reduce-adds and
@@ -931,19 +972,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
           pend_q = s;
           par_q = use & 1;
         }
+        if constexpr (!kStatsW0) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          rm[j] = nm[j];
-          rl[j] = nl[j];
-          rd[j] = nd[j];
-        }
-        load_stats(k + 1, nm, nl, nd);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // log2 of the softmax denominator, exp(x - m) / l = 2^(x*log2e - lse2)
-          // stored negated: the softmax adds them with packed FMAs / adds
-          st_lse[s * 128 + lane + 32 * j] = -(rm[j] * 1.4426950408889634f + (p.stats_lse ? 0.f : __log2f(rl[j])));
-          st_D[s * 128 + lane + 32 * j] = -rd[j];
+          for (int j = 0; j < 4; ++j) {
+            rm[j] = nm[j];
+            rl[j] = nl[j];
+            rd[j] = nd[j];
+          }
+          load_stats(k + 1, nm, nl, nd);
+          store_stats(s, rm, rl, rd);
         }
         if (!mbar_wait(bar(B_Q_FULL0 + s), use & 1, abort, status)) break;
         pend_q = -1;
