@@ -89,7 +89,7 @@ enum {
   B_DO_FULL0 = B_Q_EMPTY0 + 3,
   B_DO_FULL1, B_DO_READY0, B_DO_READY1, B_DO_EMPTY0, B_DO_EMPTY1,
   B_S_FULL, B_DP_FULL, B_P_READY, B_P_USED, B_DS_READY, B_DS_FREE, B_DQ_FULL, B_DQ_EMPTY, B_ACC_FULL,
-  B_TEARDOWN, B_EPI0, B_EPI1, B_Q_ISSUED, B_ST_READY0, B_ST_READY1, B_ST_READY2, NUM_BARS
+  B_TEARDOWN, B_EPI0, B_EPI1, B_Q_ISSUED0, B_Q_ISSUED1, B_ST_READY0, B_ST_READY1, B_ST_READY2, NUM_BARS
 };
 
 // Where a dQ partial lives on its way to TMA.  d = 128: tensor memory is
@@ -447,7 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     mbar_init(bar(B_TEARDOWN), 1);
     mbar_init(bar(B_EPI0), 128);   // dV / dK tile staged by its warpgroup
     mbar_init(bar(B_EPI1), 128);
-    mbar_init(bar(B_Q_ISSUED), 1); // (d = 128, atomic) the next Q load is issued
+    // (d = 128, atomic, no mask) the next Q load is issued; two, by block
+    // parity, so that warp 12 cannot complete the phase of block i + 1
+    // before warps 13-15 have waited for that of block i
+    mbar_init(bar(B_Q_ISSUED0), 1);
+    mbar_init(bar(B_Q_ISSUED1), 1);
     mbar_init_fence();
   }
   if (warp == 1) {
@@ -903,9 +907,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                                 bar(B_Q_FULL0 + k % NQS));
                   last_q = kn;
                 }
-                mbar_arrive(bar(B_Q_ISSUED));
+                mbar_arrive(bar(B_Q_ISSUED0 + (k & 1)));
               }
-            } else if (!mbar_wait(bar(B_Q_ISSUED), k & 1, abort, status)) {
+            } else if (!mbar_wait(bar(B_Q_ISSUED0 + (k & 1)), (k >> 1) & 1, abort, status)) {
               break;
             }
             __syncwarp();

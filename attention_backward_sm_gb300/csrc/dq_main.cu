@@ -63,7 +63,8 @@ enum {
   B_Q_FULL = 0, B_Q_READY,
   B_K_FULL0, B_K_READY0 = B_K_FULL0 + 3, B_K_EMPTY0 = B_K_READY0 + 3,   // up to 3 K stages
   B_V_FULL0 = B_K_EMPTY0 + 3, B_V_EMPTY0 = B_V_FULL0 + 3,
-  B_S_FULL = B_V_EMPTY0 + 3, B_P_DONE, B_DP_FULL0, B_DP_FULL1, B_DS_READY, B_DQ_DONE0, B_DQ_DONE1, B_ACC_FULL,
+  B_S_FULL = B_V_EMPTY0 + 3, B_P_DONE, B_DP_FULL0, B_DP_FULL1, B_DS_READY0, B_DS_READY1, B_DQ_DONE0, B_DQ_DONE1,
+  B_ACC_FULL,
   B_TEARDOWN, NUM_BARS
 };
 
@@ -282,7 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
     mbar_init(bar(B_P_DONE), 256);
     mbar_init(bar(B_DP_FULL0), 1);
     mbar_init(bar(B_DP_FULL1), 1);
-    mbar_init(bar(B_DS_READY), 256);
+    // one per dP buffer: the MMA warp issues dP_{j+1} before it waits for
+    // dS_j, so with a single barrier the softmax could complete dS_{j+1}
+    // (its next phase) before that wait had seen dS_j
+    mbar_init(bar(B_DS_READY0), 256);
+    mbar_init(bar(B_DS_READY1), 256);
     mbar_init(bar(B_DQ_DONE0), 1);
     mbar_init(bar(B_DQ_DONE1), 1);
     mbar_init(bar(B_ACC_FULL), 1);
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         issue_dp(j + 1);
       }
       // acc += dS_j K_j, dS_j read from dP buffer j & 1
-      if (!mbar_wait(bar(B_DS_READY), j & 1, abort, status)) { ok = false; break; }
+      if (!mbar_wait(bar(B_DS_READY0 + (j & 1)), (j >> 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       const int sk = j % KS;
       if (elect_one()) {
@@ -487,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         softmax_ds<false>(t_dp, neg_D, P);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_DS_READY));
+      mbar_arrive(bar(B_DS_READY0 + (j & 1)));
     }
     // ------------------------------------------------------------ epilogue
     // Warpgroup g stores head dims [g D/2, (g+1) D/2) of its rows.
