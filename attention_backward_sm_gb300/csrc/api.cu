@@ -126,6 +126,63 @@ int make_map(CUtensorMap* m, const void* base, int rows, int heads, int head_dim
   return FA_OK;
 }
 
+// Unique id of the calling thread's current context (0 if unavailable).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// A second stream of the device, with the events that fork it from and
+// join it back into a caller's stream.  It belongs to the context that was
+// current when it was made: a call from another context (or after the
+// device was reset, which makes a new context) makes new ones and leaves
+// the old handles alone.  Guarded by g_side_mu, which is held from the fork
+// to the join so that concurrent calls cannot interleave their events.
+struct SideStream {
+  unsigned long long ctx_id = 0;
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+SideStream* side_stream_locked(int dev) {
+  if (dev < 0 || dev >= 64) return nullptr;
+  const unsigned long long id = current_context_id();
+  if (id == 0) return nullptr;
+  SideStream& ss = g_side[dev];
+  if (ss.st && ss.ctx_id == id) return &ss;
+  SideStream fresh;
+  fresh.ctx_id = id;
+  if (cudaStreamCreateWithFlags(&fresh.st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+  if (cudaEventCreateWithFlags(&fresh.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&fresh.join, cudaEventDisableTiming) != cudaSuccess) {
+    if (fresh.fork) cudaEventDestroy(fresh.fork);
+    cudaStreamDestroy(fresh.st);
+    return nullptr;
+  }
+  ss = fresh;
+  return &ss;
+}
+
 int check_device() {
   static std::atomic<unsigned long long> ok_mask{0};   // devices already found to be sm_103
   int dev = 0;
@@ -391,9 +448,35 @@ int bwd_impl(const fa_bf16* q, const fa_bf16* k, const fa_bf16* v, const fa_bf16
     e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, true, s);
   } else {
     // deterministic: dK and dV from the key-block-outer kernel, dQ from the
-    // query-block-outer one (each row summed by one CTA in a fixed order)
-    e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, false, s);
-    if (e == cudaSuccess && max_q > 0) e = fa::launch_dq(p, head_dim, batch, max_kv, s);
+    // query-block-outer one (each row summed by one CTA in a fixed order).
+    // The two are independent: the dQ kernel runs on a second stream,
+    // forked from and joined back into the caller's, so that its CTAs fill
+    // the SMs the other kernel's last wave leaves idle.  Under stream
+    // capture, or without a second stream, both run in order on `s`.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream* side = (cap == cudaStreamCaptureStatusNone && max_q > 0) ? side_stream_locked(dev) : nullptr;
+    if (side == nullptr) {
+      e = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, false, s);
+      if (e == cudaSuccess && max_q > 0) e = fa::launch_dq(p, head_dim, batch, max_kv, s);
+    } else {
+      e = cudaEventRecord(side->fork, s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
+      if (e == cudaSuccess) {
+        const cudaError_t e_dq = fa::launch_dq(p, head_dim, batch, max_kv, side->st);
+        const cudaError_t e_kv = fa::launch_bwd_main(p, head_dim, batch, (max_kv + 127) / 128, false, s);
+        // the caller's stream waits for the dQ kernel, whatever happened
+        cudaError_t e_join = cudaEventRecord(side->join, side->st);
+        if (e_join == cudaSuccess) e_join = cudaStreamWaitEvent(s, side->join, 0);
+        if (e_join != cudaSuccess) cudaStreamSynchronize(side->st);
+        e = e_dq != cudaSuccess ? e_dq : (e_kv != cudaSuccess ? e_kv : e_join);
+      }
+    }
   }
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
   return ok();

@@ -68,7 +68,12 @@ enum fa_dq_mode {
     FA_DQ_DETERMINISTIC = 1   /* bitwise reproducible dQ.  head_dim 64 / 128: the key-block-outer
                                  kernel computes dK and dV only, and a query-block-outer kernel sums
                                  each row of dQ in one CTA in ascending key-block order (no atomics,
-                                 no waits between CTAs, no workspace).  head_dim 256: dQ partials
+                                 no waits between CTAs, no workspace).  The two kernels are
+                                 independent: the dQ kernel runs on a second stream that the library
+                                 keeps per device and context, forked from `stream` and joined back
+                                 into it with events (calls stay ordered on `stream`; while `stream`
+                                 is being captured into a graph, both run in order on it).
+                                 head_dim 256: dQ partials
                                  added in a fixed key-block order through counters in
                                  fa_bwd_workspace_size() bytes of workspace */
 };
