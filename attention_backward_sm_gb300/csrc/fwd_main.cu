@@ -50,7 +50,7 @@ constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (factor 256)
 
 enum {
   B_Q_FULL = 0, B_KV_FULL0, B_KV_FULL1, B_KV_EMPTY0, B_KV_EMPTY1,
-  B_S_FULL0, B_S_FULL1, B_P_READY, B_O_DONE, B_TEARDOWN, NUM_BARS
+  B_S_FULL0, B_S_FULL1, B_P_READY0, B_P_READY1, B_O_DONE, B_TEARDOWN, NUM_BARS
 };
 
 // Tiles are stored as 64-column (128-byte) chunks of `rows` rows each, as
@@ -194,7 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       mbar_init(bar(B_KV_EMPTY0 + s), 1);
       mbar_init(bar(B_S_FULL0 + s), 1);
     }
-    mbar_init(bar(B_P_READY), 128);
+    // one per score buffer: the MMA warp issues S_{j+1} before it waits for
+    // P_j, so with a single barrier the softmax could complete P_{j+1} (its
+    // next phase) before that wait had seen P_j
+    mbar_init(bar(B_P_READY0), 128);
+    mbar_init(bar(B_P_READY1), 128);
     mbar_init(bar(B_O_DONE), 1);
     mbar_init(bar(B_TEARDOWN), 1);
     mbar_init_fence();
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         }
         __syncwarp();
       }
-      if (!mbar_wait(bar(B_P_READY), j & 1, abort, status)) { ok = false; break; }
+      if (!mbar_wait(bar(B_P_READY0 + s), (j >> 1) & 1, abort, status)) { ok = false; break; }
       tc_fence_after();
       if (elect_one()) {
         const uint32_t sV = sbase + L::V + s * L::TILE_KV;
@@ -410,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_P_READY));
+      mbar_arrive(bar(B_P_READY0 + s));
     }
     ok = __all_sync(0xffffffffu, ok);
     // ------------------------------------------------------------ epilogue

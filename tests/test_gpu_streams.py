@@ -105,3 +105,44 @@ def test_deterministic_calls_in_flight_on_two_streams_from_two_threads():
         for res in got:
             for a, b in zip(plain, res):
                 assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("head_dim", [64, 256])
+def test_forward_calls_in_flight_on_two_streams_from_two_threads(head_dim):
+    """The one-tile forward (head_dim 64 / 256) from two threads on two
+    streams at once: every (O, m, l) equals a plain call's bits."""
+    import attention_backward_sm_gb300 as fab
+    case = si.fixed(f"streams_fwd_d{head_dim}", 2, 4, head_dim, 1024, 1024, True, 93)
+    dev = torch.device("cuda")
+    q, k, v, _ = (t.to(dev) for t in case.tensors())
+    cu_q = torch.from_numpy(case.cu_q).to(dev)
+    cu_kv = torch.from_numpy(case.cu_kv).to(dev)
+    plain = fab.forward_stats(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal, case.softmax_scale)
+    results = {}
+    errors = []
+
+    def worker(tid):
+        try:
+            stream = torch.cuda.Stream()
+            got = []
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    got.append(fab.forward_stats(q, k, v, cu_q, cu_kv, case.cu_q, case.cu_kv, case.causal,
+                                                 case.softmax_scale, stream=stream, check=False))
+            stream.synchronize()
+            results[tid] = got
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    fab.fa_check_device_status()
+    for got in results.values():
+        for res in got:
+            for a, b in zip(plain, res):
+                assert torch.equal(a, b)
